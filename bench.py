@@ -1,0 +1,445 @@
+#!/usr/bin/env python3
+"""Benchmark of the output-centric ("warp decode") MoE decode layer on GB300.
+
+One step = one MoE-layer decode call (moe_gate_up + moe_down through the C
+ABI) over one batch of B synthetic tokens. Default workload: the
+Qwen-3-30B-A3B-shaped layer (H=2048, I=768, E=128, top-8) at B=32 decode
+tokens with independent uniform routing per token -- the pages' bandwidth
+headline point ("Better MoE model inference with warp decode", Key claims
+[§Hardware Efficiency]: 3.95 TB/s at B=32 on B200).
+
+L2 hygiene: two different layers' MXFP8 weights (2 x 623 MB, far above the
+126 MB L2) alternate step by step, and every step uses a different batch of
+tokens, so no step finds its weights in L2 (a real decode step also reads a
+different layer's weights each time).
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU oracle
+instead (on the host cores, bounded sample per step). Multi-GPU: one process
+per GPU via torch.distributed.run; each rank runs an independent replica on
+its own batches (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+REPO = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, REPO)
+
+N_LAYERS = 2        # distinct weight sets alternated per step
+N_BATCHES = 8       # distinct token batches cycled per step
+METRIC = "MoE-layer decode tokens/s and achieved HBM GB/s (% of GB300 peak) at B=1..64"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="q30_b32")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work the oracle baseline sample aims at")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- accounting --
+
+def expert_bytes(s) -> int:
+    """MXFP8 bytes of one expert: 3*H*I E4M3 codes + 3*H*I/32 E8M0 scales."""
+    return 3 * s.H * s.I + 3 * s.H * s.I // 32
+
+
+def gate_up_bytes(s, ids: np.ndarray) -> int:
+    """Algorithmic bytes of one moe_gate_up launch: unique touched experts'
+    gate+up codes and scales, x, ids, and the BF16 intermediate written."""
+    B, k = ids.shape
+    U = len(np.unique(ids))
+    return U * (2 * s.H * s.I + 2 * s.H * s.I // 32) + B * s.H * 2 + B * k * 4 + B * k * s.I * 2
+
+
+def down_bytes(s, ids: np.ndarray) -> int:
+    """Algorithmic bytes of one moe_down launch: unique touched experts' down
+    codes and scales, the intermediate read, ids, weights and y written."""
+    B, k = ids.shape
+    U = len(np.unique(ids))
+    return U * (s.H * s.I + s.H * s.I // 32) + B * k * s.I * 2 + B * k * 8 + B * s.H * 4
+
+
+def layer_bytes(s, ids) -> int:
+    return gate_up_bytes(s, ids) + down_bytes(s, ids)
+
+
+def measured_peaks():
+    p = os.path.join(REPO, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_sha() -> str:
+    src = os.path.join(REPO, "output_centric_expert_gb300", "csrc", "warp_decode.cu")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(REPO, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(kernel, {}).get(workload)
+    if not ent or ent.get("kernel_sha") != kernel_source_sha():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------- workload setup --
+
+def build_device_layers(shape, n_layers, seed, device):
+    from concurrent.futures import ThreadPoolExecutor
+
+    from output_centric_expert_gb300 import ops, workload
+    sh = ops.make_shape(shape.H, shape.I, shape.E, shape.top_k)
+    layers = []
+    for layer in range(n_layers):
+        packed = ops.empty_packed_host(sh)
+
+        def one(e):
+            g, u, d = workload.expert_weights(shape, e, seed, layer)
+            ops.moe_pack_weights(sh, g[None], u[None], d[None], out=packed, expert_offset=e)
+
+        with ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
+            list(ex.map(one, range(shape.E)))
+        layers.append(ops.DeviceWeights(sh, packed, device))
+    return layers
+
+
+def make_batches(wl, n, seed):
+    from output_centric_expert_gb300 import workload
+    return [workload.tokens(wl.shape, wl.B, seed=seed, batch=b, routing=wl.routing) for b in range(n)]
+
+
+# -------------------------------------------------------------- CPU oracle --
+
+def oracle_baseline(wl, seconds: float, seed: int = 0):
+    """Time the oracle (single-threaded FP64 C) on whole batches of the
+    workload until about `seconds` of CPU work. Returns tokens/s and sample."""
+    import oracle
+    from output_centric_expert_gb300 import workload
+    batches = make_batches(wl, 4, seed)
+    need = np.unique(np.concatenate([b[1].ravel() for b in batches]))
+    ref = _oracle_layer(wl.shape, seed, 0, need)
+    tokens = 0
+    t0 = time.perf_counter()
+    i = 0
+    while True:
+        x, ids, w = batches[i % len(batches)]
+        oracle.moe_layer(ref, x, ids, w)
+        tokens += wl.B
+        i += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or i >= 64:
+            break
+    return tokens / el, f"{i} batches x {wl.B} tokens of {wl.name} (layer 0), {el:.1f} s"
+
+
+def _oracle_layer(shape, seed, layer, experts):
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    from output_centric_expert_gb300 import workload
+    E, I, H = shape.E, shape.I, shape.H
+    gc = np.zeros((E, I, H), np.uint8)
+    gs = np.zeros((E, I, H // 32), np.uint8)
+    uc, us = np.zeros_like(gc), np.zeros_like(gs)
+    dc = np.zeros((E, H, I), np.uint8)
+    ds = np.zeros((E, H, I // 32), np.uint8)
+
+    def one(e):
+        g, u, d = workload.expert_weights(shape, int(e), seed, layer)
+        gc[e], gs[e] = oracle.quantize_mxfp8(g)
+        uc[e], us[e] = oracle.quantize_mxfp8(u)
+        dc[e], ds[e] = oracle.quantize_mxfp8(d)
+
+    with ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
+        list(ex.map(one, experts))
+    return oracle.QuantizedLayer(gc, gs, uc, us, dc, ds)
+
+
+def run_reference(args, wl, rank):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    per_step_tokens = max(1, min(wl.B, 2))  # bounded sample of each step's batch
+    batches = make_batches(wl, N_BATCHES, 0)
+    need = np.unique(np.concatenate([b[1][:per_step_tokens].ravel() for b in batches]))
+    ref = _oracle_layer(wl.shape, 0, 0, need)
+    for s in range(args.warmup):
+        x, ids, w = batches[s % N_BATCHES]
+        oracle.moe_layer(ref, x[:per_step_tokens], ids[:per_step_tokens], w[:per_step_tokens])
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        x, ids, w = batches[s % N_BATCHES]
+        oracle.moe_layer(ref, x[:per_step_tokens], ids[:per_step_tokens], w[:per_step_tokens])
+    el = time.perf_counter() - t0
+    value = per_step_tokens * args.steps / el
+    sample = f"{per_step_tokens} of the {wl.B} tokens of each step's batch"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "H": wl.shape.H, "I": wl.shape.I, "E": wl.shape.E,
+                   "top_k": wl.shape.top_k, "B": wl.B, "routing": wl.routing},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm --
+
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from output_centric_expert_gb300 import ops
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    s = wl.shape
+    seed = 0
+    layers = build_device_layers(s, N_LAYERS, seed, dev)
+    batches = make_batches(wl, N_BATCHES, seed + 1000 * rank)
+    dx = [torch.from_numpy(b[0].view(np.int16)).to(dev) for b in batches]
+    dids = [torch.from_numpy(b[1]).to(dev) for b in batches]
+    dw = [torch.from_numpy(b[2]).to(dev) for b in batches]
+    h = torch.empty((wl.B, s.top_k, s.I), dtype=torch.int16, device=dev)
+    y = torch.empty((wl.B, s.H), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        b = i % N_BATCHES
+        ops.moe_layer(layers[i % N_LAYERS], dx[b], dids[b], dw[b], h, y, err, stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(v: float) -> float:
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    barrier()
+
+    # ---- main timed region: K whole-layer steps --------------------------
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local_rank)
+    with ClockSampler(gpu_id) as clk:
+        barrier()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        barrier()
+    el_ms = max_over_ranks(ev0.elapsed_time(ev1))
+    ms_per_step = el_ms / args.steps
+    value = wl.B * world * args.steps / (el_ms / 1e3)
+    if int(err.item()) != 0:
+        raise RuntimeError("device error flag set: an expert id was out of range")
+
+    # ---- per-kernel durations (same steps, an event between the kernels) --
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        b = i % N_BATCHES
+        L = layers[i % N_LAYERS]
+        evs[i][0].record(stream)
+        ops.moe_gate_up(L, dx[b], dids[b], h, err, stream)
+        evs[i][1].record(stream)
+        ops.moe_down(L, h, dids[b], dw[b], y, err, stream)
+        evs[i][2].record(stream)
+    barrier()
+    gu_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    gu_bytes = [gate_up_bytes(s, batches[i % N_BATCHES][1]) for i in range(args.steps)]
+    dn_bytes = [down_bytes(s, batches[i % N_BATCHES][1]) for i in range(args.steps)]
+    lay_bytes = [a + b for a, b in zip(gu_bytes, dn_bytes)]
+    peak, peak_kind = measured_peaks()
+    gu_gbs = sum(gu_bytes) / (sum(gu_ms) / 1e3) / 1e9
+    dn_gbs = sum(dn_bytes) / (sum(dn_ms) / 1e3) / 1e9
+    layer_gbs = sum(lay_bytes) / args.steps / (ms_per_step / 1e3) / 1e9
+
+    # ---- end to end from pinned host buffers (copies inside the region) ----
+    px = [torch.from_numpy(b[0].view(np.int16)).pin_memory() for b in batches]
+    pids = [torch.from_numpy(b[1]).pin_memory() for b in batches]
+    pw = [torch.from_numpy(b[2]).pin_memory() for b in batches]
+    py = torch.empty((wl.B, s.H), dtype=torch.float32).pin_memory()
+    sx = torch.empty_like(dx[0])
+    sids = torch.empty_like(dids[0])
+    sw = torch.empty_like(dw[0])
+
+    def e2e_step(i):
+        b = i % N_BATCHES
+        ops.moe_layer_host(layers[i % N_LAYERS], px[b], pids[b], pw[b], sx, sids, sw, h, y, py,
+                           err, stream)
+
+    for i in range(3):
+        e2e_step(i)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    e2e_value = wl.B * world * args.steps / (e2e_ms / 1e3)
+    h2d = px[0].numel() * 2 + pids[0].numel() * 4 + pw[0].numel() * 4
+    d2h = py.numel() * 4
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, sample = oracle_baseline(wl, args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
+    traffic = ncu_traffic("moe_gate_up", wl.name)
+    gu_launch_bytes = sum(gu_bytes) / args.steps
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "H": s.H, "I": s.I, "E": s.E, "top_k": s.top_k,
+                   "B": wl.B, "routing": wl.routing, "parallelism": f"replicas x{world}",
+                   "formats": "MXFP8 (E4M3 + E8M0/32) weights, BF16 x and h, FP32 accumulators and y",
+                   "l2": f"inputs larger than L2: {N_LAYERS} layers' weights "
+                         f"({N_LAYERS * layers[0].nbytes / 1e9:.2f} GB) alternate per step, "
+                         f"{N_BATCHES} token batches cycle",
+                   "layer_gbs": layer_gbs, "layer_frac_of_peak": layer_gbs / peak,
+                   "layer_bytes_per_step": sum(lay_bytes) / args.steps,
+                   "gate_up_us": sum(gu_ms) / args.steps * 1e3,
+                   "down_us": sum(dn_ms) / args.steps * 1e3,
+                   "down_gbs": dn_gbs},
+        "roofline": {"bound": "hbm", "kernel": "moe_gate_up", "achieved": gu_gbs, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": gu_gbs / peak,
+                     "algorithmic_bytes_per_launch": gu_launch_bytes,
+                     "traffic": traffic},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    from output_centric_expert_gb300 import workload
+    wl = workload.WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        if world == 1 and args.gpus > 1:
+            raise SystemExit("--gpus N > 1 needs torch.distributed.run with N processes")
+    if args.impl == "reference":
+        run_reference(args, wl, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, wl, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

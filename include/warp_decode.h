@@ -1,0 +1,161 @@
+/*
+ * warp_decode.h -- C ABI of the GB300-native output-centric ("warp decode")
+ * MoE decode layer.
+ *
+ * The method ("Better MoE model inference with warp decode", TL;DR, Key claims
+ * [§Reorganized parallelism] and [§How the two kernels work], Method; sd114.wiki
+ * "Warp Decode" page, section 技术原理：两个 Kernel 搞定一切): for decode-time
+ * MoE at small batch, give each warp one output scalar. The layer is two
+ * kernels:
+ *   moe_gate_up : one warp per (token, routed expert, intermediate neuron);
+ *                 gate and up dot products share one read of the BF16
+ *                 activation, MXFP8 weights are decoded to FP32 on the fly,
+ *                 SiLU(gate)*up is written out as BF16.
+ *   moe_down    : one warp per (token, output dim); one FP32 accumulator is
+ *                 streamed over all top-k experts' down rows with the routing
+ *                 weight folded in, then reduced across the 32 lanes by a
+ *                 butterfly shuffle. No per-expert output buffer exists.
+ *
+ * Numerics (fixed by this API):
+ *   g = sum_h x[t,h] Wg[e,n,h],  u = sum_h x[t,h] Wu[e,n,h]     (FP32 accum.)
+ *   h[t,j,n] = bf16_rne( silu(g) * u ),  silu(g) = g / (1 + exp(-g))
+ *   y[t,o]   = sum_j w[t,j] * sum_i h[t,j,i] Wd[e_j,o,i]          (FP32 accum.)
+ * with MXFP8 weights (OCP MX v1.0): E4M3 codes, one E8M0 scale per 32
+ * consecutive elements along the reduction axis (H for gate/up, I for down).
+ *
+ * Conventions for every entry point:
+ *  - Shapes: H % 32 == 0, I % 32 == 0, E >= 1, 1 <= top_k <= E, B >= 0.
+ *    B == 0 is a valid empty batch: nothing is launched, MOE_OK is returned.
+ *  - Device pointers: caller-owned (e.g. torch allocations). Weight, x and h
+ *    pointers must be 16-byte aligned; ids, w and y 4-byte aligned.
+ *  - The library allocates no device memory, never synchronises, and enqueues
+ *    its work on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *  - Host-detectable problems (null pointer, bad shape, misalignment) return
+ *    an error before anything is launched. A failed launch returns
+ *    MOE_ERR_CUDA; moe_last_error() describes the last failure on this thread.
+ *  - Expert ids are not checked on the host (that would need a copy back): a
+ *    slot whose id is outside [0, E) contributes nothing, its intermediate is
+ *    0, and if err_flag is non-NULL the device int32 *err_flag gets bit 0 set
+ *    (it is never cleared by the library).
+ *  - Duplicate ids in one token are allowed; their contributions add.
+ *  - Device code has no traps, asserts or waits on flags.
+ */
+#ifndef WARP_DECODE_H
+#define WARP_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL = 1,        /* a required pointer is NULL */
+  MOE_ERR_SHAPE = 2,       /* shape or batch outside the supported range */
+  MOE_ERR_ALIGN = 3,       /* a pointer is not aligned as documented */
+  MOE_ERR_CUDA = 4,        /* a CUDA call or kernel launch failed */
+  MOE_ERR_UNSUPPORTED = 5  /* valid request this build does not implement */
+} moe_status;
+
+/* Layer shape: hidden size H, intermediate size I, E experts, top_k per token. */
+typedef struct {
+  int32_t H, I, E, top_k;
+} moe_shape;
+
+/*
+ * Packed MXFP8 expert weights, device memory, written by moe_pack_weights:
+ *   gu_codes  [E][I][2][H]    uint8 E4M3: for neuron n of expert e, the gate
+ *                             row (H codes) followed by the up row (H codes),
+ *                             so one warp streams one contiguous 2H-byte run.
+ *   gu_scales [E][I][2][H/32] uint8 E8M0, same order (gate scales, up scales).
+ *   d_codes   [E][H][I]       uint8 E4M3: down row o of expert e is contiguous.
+ *   d_scales  [E][H][I/32]    uint8 E8M0.
+ * Scale b of a row applies to elements 32b .. 32b+31 of that row.
+ */
+typedef struct {
+  const uint8_t* gu_codes;
+  const uint8_t* gu_scales;
+  const uint8_t* d_codes;
+  const uint8_t* d_scales;
+} moe_weights;
+
+/* Which packed array moe_packed_bytes sizes. */
+enum { MOE_GU_CODES = 0, MOE_GU_SCALES = 1, MOE_D_CODES = 2, MOE_D_SCALES = 3 };
+
+/* Bytes of packed array `which` for `shape` (all E experts); 0 if the shape
+ * is invalid or `which` unknown. */
+size_t moe_packed_bytes(const moe_shape* shape, int which);
+
+/*
+ * Quantise FP32 expert weights to MXFP8 and write the packed layout above.
+ * Host memory in and out (runs on the CPU, no CUDA call). Inputs:
+ *   w_gate [E][I][H], w_up [E][I][H], w_down [E][H][I]  (row-major FP32).
+ * Rule (OCP MX v1.0 conversion): per 32-element block, shared exponent
+ * floor(log2(max|v|)) - 8, stored as E8M0 (clamped to [0, 254]; an all-zero
+ * block stores 0); elements v / 2^shared_exp rounded to nearest E4M3, ties to
+ * even, magnitudes above 448 saturated to 448. Any `shape->E` works, so a
+ * caller may pack one expert at a time (E = 1) into the matching offsets.
+ */
+moe_status moe_pack_weights(const moe_shape* shape, const float* w_gate, const float* w_up,
+                            const float* w_down, uint8_t* gu_codes, uint8_t* gu_scales,
+                            uint8_t* d_codes, uint8_t* d_scales);
+
+/*
+ * moe_gate_up -- first kernel ("moe_gate_up_3d_batched" on the pages).
+ *   x    [B][H]        BF16 activations (device)
+ *   ids  [B][top_k]    int32 expert ids (device)
+ *   h    [B][top_k][I] BF16 intermediate, written (device)
+ * h[t,j,n] = bf16_rne(silu(g)*u) for expert ids[t,j]; 0 for an invalid id.
+ */
+moe_status moe_gate_up(const moe_shape* shape, const moe_weights* w, const uint16_t* x,
+                       const int32_t* ids, int32_t B, uint16_t* h, int32_t* err_flag,
+                       void* stream);
+
+/*
+ * moe_down -- second kernel ("moe_down_3d_batched" on the pages).
+ *   h    [B][top_k][I] BF16 intermediate from moe_gate_up (device)
+ *   ids  [B][top_k]    int32 expert ids (device)
+ *   wts  [B][top_k]    FP32 routing weights (device)
+ *   y    [B][H]        FP32 output, overwritten (device)
+ * y[t,o] = sum_j wts[t,j] * sum_i h[t,j,i] * Wd[ids[t,j], o, i].
+ */
+moe_status moe_down(const moe_shape* shape, const moe_weights* w, const uint16_t* h,
+                    const int32_t* ids, const float* wts, int32_t B, float* y,
+                    int32_t* err_flag, void* stream);
+
+/*
+ * moe_layer -- the whole layer: moe_gate_up then moe_down on `stream`.
+ * h_scratch [B][top_k][I] BF16 is caller-provided device memory that holds
+ * the intermediate between the two kernels (its contents afterwards are the
+ * intermediate, as from moe_gate_up).
+ */
+moe_status moe_layer(const moe_shape* shape, const moe_weights* w, const uint16_t* x,
+                     const int32_t* ids, const float* wts, int32_t B, uint16_t* h_scratch,
+                     float* y, int32_t* err_flag, void* stream);
+
+/*
+ * moe_layer_host -- the layer end to end from HOST buffers: copies x, ids and
+ * wts host->device into the caller's device staging buffers (one
+ * cudaMemcpyAsync each), runs moe_layer, and copies y device->host, all
+ * enqueued on `stream`. Returns once enqueued: synchronise `stream` before
+ * reading y_host. Host buffers should be pinned for the copies to be
+ * asynchronous. Shapes and device-buffer rules as for moe_layer.
+ */
+moe_status moe_layer_host(const moe_shape* shape, const moe_weights* w, const uint16_t* x_host,
+                          const int32_t* ids_host, const float* wts_host, int32_t B,
+                          uint16_t* x_dev, int32_t* ids_dev, float* wts_dev, uint16_t* h_dev,
+                          float* y_dev, float* y_host, int32_t* err_flag, void* stream);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status status);
+
+/* Description of the last failure on the calling thread ("" if none). */
+const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WARP_DECODE_H */

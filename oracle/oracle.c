@@ -156,14 +156,14 @@ static uint8_t e4m3_nearest(double v) {
   int lo = 0, hi = 0x7E;
   while (lo < hi) {
     int mid = (lo + hi + 1) / 2;
-    if (oracle_e4m3_value((uint8_t)mid) <= a)
+    if (e4m3_table[mid] <= a)
       lo = mid;
     else
       hi = mid - 1;
   }
-  double below = oracle_e4m3_value((uint8_t)lo);
+  double below = e4m3_table[lo];
   if (below == a) return (uint8_t)(sign | lo);
-  double above = oracle_e4m3_value((uint8_t)(lo + 1));
+  double above = e4m3_table[lo + 1];
   double d_lo = a - below, d_hi = above - a;
   int pick;
   if (d_lo < d_hi)
@@ -178,6 +178,7 @@ static uint8_t e4m3_nearest(double v) {
 int oracle_quantize_mxfp8(const float* w, int64_t rows, int64_t K, uint8_t* codes,
                           uint8_t* scales) {
   if (K % 32 != 0 || rows < 0) return -1;
+  fill_tables();
   int64_t nb = K / 32;
   for (int64_t r = 0; r < rows; ++r) {
     for (int64_t b = 0; b < nb; ++b) {

@@ -1,0 +1,116 @@
+"""The C-ABI library without a GPU: symbols, host-side validation, the packer."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from output_centric_expert_gb300 import ops, workload
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "warp_decode.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    declared = _declared_functions()
+    assert "moe_gate_up" in declared and "moe_down" in declared and "moe_layer" in declared
+    L = ops.lib()
+    for name in declared:
+        assert hasattr(L, name), f"{name} declared in warp_decode.h but not exported"
+    assert sorted(ops.exported_symbols()) == declared
+
+
+def _fake_weights(aligned=True):
+    base = 0x10000 if aligned else 0x10001
+    return ops.MoeWeights(base, base + 0x1000, base + 0x2000, base + 0x3000)
+
+
+def test_host_validation_rejects_before_launch():
+    """Bad arguments return an error code and launch nothing (no GPU needed)."""
+    L = ops.lib()
+    sh = ops.make_shape(256, 128, 8, 2)
+    w = _fake_weights()
+    P = 0x20000  # 16-byte aligned fake device address (never dereferenced)
+
+    def gate_up(shape, weights, x, ids, B, h, err=None):
+        return L.moe_gate_up(ctypes.byref(shape) if shape else None,
+                             ctypes.byref(weights) if weights else None, x, ids, B, h, err, None)
+
+    assert gate_up(None, w, P, P, 1, P) == 1  # MOE_ERR_NULL
+    assert gate_up(sh, None, P, P, 1, P) == 1
+    assert gate_up(sh, w, None, P, 1, P) == 1
+    for bad in ((250, 128, 8, 2), (256, 100, 8, 2), (256, 128, 0, 1), (256, 128, 8, 9), (256, 128, 8, 0)):
+        assert gate_up(ops.make_shape(*bad), w, P, P, 1, P) == 2  # MOE_ERR_SHAPE
+    assert gate_up(sh, w, P, P, -1, P) == 2
+    assert gate_up(sh, _fake_weights(aligned=False), P, P, 1, P) == 3  # MOE_ERR_ALIGN
+    assert gate_up(sh, w, P + 2, P, 1, P) == 3
+    assert gate_up(sh, w, P, P, 1, P + 8) == 3
+    assert gate_up(sh, w, P, P + 1, 1, P) == 3
+    # empty batch: valid, nothing launched
+    assert gate_up(sh, w, None, None, 0, None) == 0
+    assert L.moe_down(ctypes.byref(sh), ctypes.byref(w), None, None, None, 0, None, None, None) == 0
+    assert L.moe_layer(ctypes.byref(sh), ctypes.byref(w), None, None, None, 0, None, None, None, None) == 0
+    assert L.moe_down(ctypes.byref(sh), ctypes.byref(w), P, P, P + 2, 1, P, None, None) == 3
+    assert L.moe_layer(ctypes.byref(sh), ctypes.byref(w), P, P, P, 1, None, P, None, None) == 1
+    assert "shape" in ops.lib().moe_last_error().decode() or ops.lib().moe_last_error() is not None
+    assert ops.status_string(2) == "unsupported shape"
+
+
+def test_packed_sizes():
+    q30 = ops.make_shape(2048, 768, 128, 8)
+    sizes = [ops.moe_packed_bytes(q30, w) for w in range(4)]
+    assert sizes == [128 * 768 * 2 * 2048, 128 * 768 * 2 * 64, 128 * 2048 * 768, 128 * 2048 * 24]
+    per_expert = sum(sizes) // 128
+    assert per_expert == 3 * 2048 * 768 + 3 * 2048 * 768 // 32 == 4_866_048
+    assert ops.moe_packed_bytes(ops.make_shape(100, 768, 128, 8), 0) == 0
+    assert ops.moe_packed_bytes(q30, 7) == 0
+
+
+def _unpack_to_canonical(packed: ops.PackedHost, H, I, E):
+    """Product layout -> the oracle's canonical arrays (layout knowledge only)."""
+    gu = packed.gu_codes.reshape(E, I, 2, H)
+    gus = packed.gu_scales.reshape(E, I, 2, H // 32)
+    return (gu[:, :, 0], gus[:, :, 0], gu[:, :, 1], gus[:, :, 1],
+            packed.d_codes.reshape(E, H, I), packed.d_scales.reshape(E, H, I // 32))
+
+
+@pytest.mark.parametrize("H,I,E", [(256, 128, 8), (64, 96, 3), (32, 32, 1)])
+def test_packer_matches_oracle_quantizer_bit_exact(H, I, E):
+    rng = np.random.default_rng(H + I + E)
+    g = (rng.standard_normal((E, I, H)) * 0.05).astype(np.float32)
+    u = (rng.standard_normal((E, I, H)) * 0.05).astype(np.float32)
+    d = (rng.standard_normal((E, H, I)) * 0.05).astype(np.float32)
+    # edge blocks: zeros, huge, tiny, exact ties of E4M3 (1.0625 is midway 1.0/1.125)
+    g[0, 0, :32] = 0.0
+    u[0, 0, :32] *= 1e6
+    d[0, 0, :32] *= 1e-35
+    g[-1, -1, :32] = np.float32(1.0625) * (np.arange(32) % 3 - 1)
+    g[-1, -1, 0] = 448.0 / 256.0  # makes the block scale 2^-8 exactly
+    sh = ops.make_shape(H, I, E, 1)
+    packed = ops.moe_pack_weights(sh, g, u, d)
+    gc, gs, uc, us, dc, ds = _unpack_to_canonical(packed, H, I, E)
+    ref = oracle.QuantizedLayer.from_fp32(g, u, d)
+    for got, want in ((gc, ref.gate_codes), (gs, ref.gate_scales), (uc, ref.up_codes),
+                      (us, ref.up_scales), (dc, ref.down_codes), (ds, ref.down_scales)):
+        assert np.array_equal(got, want)
+
+
+def test_packer_per_expert_slices_equal_whole_pack():
+    s = workload.SHAPES["tiny"]
+    g, u, d = workload.all_weights(s, seed=5)
+    sh = ops.make_shape(s.H, s.I, s.E, s.top_k)
+    whole = ops.moe_pack_weights(sh, g, u, d)
+    parts = ops.empty_packed_host(sh)
+    for e in range(s.E):
+        ops.moe_pack_weights(sh, g[e:e + 1], u[e:e + 1], d[e:e + 1], out=parts, expert_offset=e)
+    for a, b in zip((whole.gu_codes, whole.gu_scales, whole.d_codes, whole.d_scales),
+                    (parts.gu_codes, parts.gu_scales, parts.d_codes, parts.d_scales)):
+        assert np.array_equal(a, b)

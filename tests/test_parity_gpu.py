@@ -1,0 +1,228 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 CPU oracle.
+
+Bar: per token, max |y_gpu - y_oracle| <= 4e-3 and cosine >= 0.99999 for
+unit-scale inputs (x ~ N(0,1), W ~ N(0, 0.05^2)). The BF16 intermediate h is
+also compared: a code may differ from the oracle's only where the FP32 and the
+exact value of silu(g)*u fall on different sides of a BF16 rounding boundary,
+i.e. by one BF16 step, and rarely.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from output_centric_expert_gb300 import ops, workload
+
+from ._layers import Layer, parity_stats
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 4e-3
+MIN_COS = 0.99999
+
+
+def _dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    return t.view(dtype) if dtype is not None else t
+
+
+def _run_layer(layer: Layer, x, ids, w, with_err=False):
+    B = x.shape[0]
+    k = layer.shape.top_k
+    xd, idd, wd = _dev(x.view(np.int16)), _dev(ids), _dev(w)
+    h = torch.empty((B, k, layer.shape.I), dtype=torch.int16, device="cuda")
+    y = torch.empty((B, layer.shape.H), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.moe_layer(layer.dev, xd, idd, wd, h, y, err)
+    torch.cuda.synchronize()
+    out = (y.cpu().numpy(), h.cpu().numpy().view(np.uint16))
+    return out + (int(err.item()),) if with_err else out
+
+
+def _bf16_vals(bits):
+    return workload.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def _check_h(h_gpu, h_ref, max_frac=0.01):
+    diff = h_gpu != h_ref
+    frac = float(diff.mean()) if diff.size else 0.0
+    assert frac <= max_frac, f"{frac:.4%} of intermediate codes differ"
+    if diff.any():
+        vg, vr = _bf16_vals(h_gpu[diff]), _bf16_vals(h_ref[diff])
+        step = 2.0**-7 * np.maximum(np.abs(vg), np.abs(vr)) + 1e-37
+        assert np.all(np.abs(vg - vr) <= step), "an intermediate differs by more than one BF16 step"
+
+
+def _check_y(y_gpu, y_ref):
+    d, cos = parity_stats(y_gpu, y_ref)
+    assert d <= MAX_ABS, f"max|dy| = {d:.3e}"
+    assert cos >= MIN_COS, f"min cosine = {cos:.8f}"
+    return d, cos
+
+
+# ------------------------------------------------------------ fixtures ------
+
+@pytest.fixture(scope="module")
+def tiny():
+    return Layer(workload.SHAPES["tiny"])
+
+
+@pytest.fixture(scope="module")
+def q30():
+    return Layer(workload.SHAPES["q30"])
+
+
+# ------------------------------------------------------- the named configs --
+
+def test_tiny_config_full(tiny):
+    """H=256, I=128, E=8, top-2, B=1, seed 0: every output and intermediate."""
+    x, ids, w = workload.tokens(tiny.shape, 1)
+    y, h = _run_layer(tiny, x, ids, w)
+    y_ref, h_ref, bad = oracle.moe_layer(tiny.ref, x, ids, w, return_h=True)
+    assert bad == 0
+    _check_y(y, y_ref)
+    _check_h(h, h_ref)
+
+
+@pytest.mark.parametrize("B,routing", [(1, "uniform"), (32, "uniform"), (64, "skewed"), (7, "uniform")])
+def test_q30_layer_all_tokens(q30, B, routing):
+    """Qwen-3-30B-A3B-shaped layer (H=2048, I=768, E=128, top-8), every token."""
+    x, ids, w = workload.tokens(q30.shape, B, routing=routing, batch=B)
+    y, h = _run_layer(q30, x, ids, w)
+    y_ref, h_ref, _ = oracle.moe_layer(q30.ref, x, ids, w, return_h=True)
+    _check_y(y, y_ref)
+    _check_h(h, h_ref)
+
+
+def test_q30_down_kernel_alone_on_oracle_intermediate(q30):
+    """moe_down fed the oracle's own BF16 intermediate: only summation order differs."""
+    B = 16
+    x, ids, w = workload.tokens(q30.shape, B, batch=99)
+    y_ref, h_ref, _ = oracle.moe_layer(q30.ref, x, ids, w, return_h=True)
+    y = torch.empty((B, q30.shape.H), dtype=torch.float32, device="cuda")
+    ops.moe_down(q30.dev, _dev(h_ref.view(np.int16)), _dev(ids), _dev(w), y)
+    torch.cuda.synchronize()
+    d, _ = parity_stats(y.cpu().numpy(), y_ref)
+    assert d <= 1e-4, d
+
+
+def test_q30_gate_up_kernel_alone(q30):
+    B = 8
+    x, ids, _ = workload.tokens(q30.shape, B, batch=98)
+    _, h_ref, _ = oracle.moe_layer(q30.ref, x, ids, np.ones(ids.shape, np.float32), return_h=True)
+    h = torch.empty((B, q30.shape.top_k, q30.shape.I), dtype=torch.int16, device="cuda")
+    ops.moe_gate_up(q30.dev, _dev(x.view(np.int16)), _dev(ids), h)
+    torch.cuda.synchronize()
+    _check_h(h.cpu().numpy().view(np.uint16), h_ref)
+
+
+def test_q235_sampled_tokens():
+    """Qwen-3-235B-A22B-shaped layer at B=64 (full size); the oracle checks 3 tokens."""
+    s = workload.SHAPES["q235"]
+    B = 64
+    x, ids, w = workload.tokens(s, B)
+    sample = [0, 31, 63]
+    layer = Layer(s, oracle_experts=np.unique(ids[sample]))
+    y, _ = _run_layer(layer, x, ids, w)
+    y_ref, _ = oracle.moe_layer(layer.ref, x[sample], ids[sample], w[sample])
+    _check_y(y[sample], y_ref)
+    assert np.all(np.isfinite(y))
+
+
+# ------------------------------------------------------------ edge cases ----
+
+def _rand_layer_shape(H, I, E, k, seed=0):
+    return Layer(workload.LayerShape(H, I, E, k), seed=seed)
+
+
+@pytest.mark.parametrize("H,I,E,k,B", [
+    (32, 32, 2, 1, 1),        # smallest shape: one scale block per row
+    (2080, 800, 4, 2, 3),     # several load rounds with a ragged tail on both kernels
+    (96, 160, 5, 3, 5),       # rows shorter than a warp's chunk span
+    (544, 64, 3, 3, 2),       # top_k = E
+    (256, 128, 8, 8, 4),      # tiny layer with k = E
+])
+def test_ragged_and_small_shapes(H, I, E, k, B):
+    layer = _rand_layer_shape(H, I, E, k, seed=H + I)
+    x, ids, w = workload.tokens(layer.shape, B, seed=7)
+    y, h = _run_layer(layer, x, ids, w)
+    y_ref, h_ref, _ = oracle.moe_layer(layer.ref, x, ids, w, return_h=True)
+    _check_y(y, y_ref)
+    _check_h(h, h_ref)
+
+
+def test_duplicate_ids_and_all_tokens_on_one_expert(tiny):
+    B = 16
+    x, _, _ = workload.tokens(tiny.shape, B, batch=5)
+    ids = np.full((B, 2), 3, dtype=np.int32)  # every slot -> expert 3 (duplicates within a token)
+    w = np.tile(np.array([[0.75, 0.25]], np.float32), (B, 1))
+    y, h = _run_layer(tiny, x, ids, w)
+    y_ref, h_ref, _ = oracle.moe_layer(tiny.ref, x, ids, w, return_h=True)
+    _check_y(y, y_ref)
+    _check_h(h, h_ref)
+
+
+def test_invalid_ids_flagged_and_skipped(tiny):
+    B = 3
+    x, ids, w = workload.tokens(tiny.shape, B, batch=6)
+    ids = ids.copy()
+    ids[0, 1] = 8      # == E
+    ids[2, 0] = -5
+    y, h, err = _run_layer(tiny, x, ids, w, with_err=True)
+    y_ref, h_ref, bad = oracle.moe_layer(tiny.ref, x, ids, w, return_h=True)
+    assert bad == 2 and err == 1
+    assert np.all(h[0, 1] == 0) and np.all(h[2, 0] == 0)
+    _check_y(y, y_ref)
+    _check_h(h, h_ref)
+
+
+def test_empty_batch_launches_nothing(tiny):
+    y = torch.full((0, tiny.shape.H), 7.0, device="cuda")
+    ops.moe_layer(tiny.dev, torch.empty((0, tiny.shape.H), dtype=torch.int16, device="cuda"),
+                  torch.empty((0, 2), dtype=torch.int32, device="cuda"),
+                  torch.empty((0, 2), dtype=torch.float32, device="cuda"),
+                  torch.empty((0, 2, tiny.shape.I), dtype=torch.int16, device="cuda"), y)
+    torch.cuda.synchronize()
+
+
+def test_nan_scale_propagates_to_its_outputs():
+    layer = _rand_layer_shape(64, 64, 2, 1, seed=3)
+    # NaN E8M0 scale in down row 5 of expert 1, in both the oracle and the device copy
+    layer.ref.down_scales[1, 5, 0] = 0xFF
+    d_scales = layer.dev.tensors[3].view(2, 64, 2)
+    d_scales[1, 5, 0] = 0xFF
+    x, _, _ = workload.tokens(layer.shape, 2)
+    ids = np.array([[1], [0]], np.int32)
+    w = np.ones((2, 1), np.float32)
+    y, _ = _run_layer(layer, x, ids, w)
+    y_ref, _ = oracle.moe_layer(layer.ref, x, ids, w)
+    assert np.isnan(y[0, 5]) and np.isnan(y_ref[0, 5])
+    assert np.all(np.isfinite(np.delete(y[0], 5))) and np.all(np.isfinite(y[1]))
+
+
+def test_deterministic_and_host_entry_point_matches(q30):
+    B = 32
+    x, ids, w = workload.tokens(q30.shape, B, batch=3)
+    y1, h1 = _run_layer(q30, x, ids, w)
+    y2, h2 = _run_layer(q30, x, ids, w)
+    assert np.array_equal(y1, y2) and np.array_equal(h1, h2)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    xh, idh, wh = pin(x.view(np.int16)), pin(ids), pin(w)
+    yh = torch.empty((B, q30.shape.H), dtype=torch.float32).pin_memory()
+    dev = dict(x_dev=torch.empty_like(xh, device="cuda"), ids_dev=torch.empty_like(idh, device="cuda"),
+               wts_dev=torch.empty_like(wh, device="cuda"),
+               h_dev=torch.empty((B, 8, q30.shape.I), dtype=torch.int16, device="cuda"),
+               y_dev=torch.empty((B, q30.shape.H), dtype=torch.float32, device="cuda"))
+    ops.moe_layer_host(q30.dev, xh, idh, wh, y_host=yh, **dev)
+    torch.cuda.synchronize()
+    assert np.array_equal(yh.numpy(), y1)
+
+
+def test_library_allocates_no_device_memory(tiny):
+    free0, _ = torch.cuda.mem_get_info()
+    x, ids, w = workload.tokens(tiny.shape, 4)
+    for _ in range(3):
+        _run_layer(tiny, x, ids, w)
+    free1, _ = torch.cuda.mem_get_info()
+    # only torch's caching allocator may have grown (the test's own tensors)
+    assert free0 - free1 < 64 << 20
