@@ -2,9 +2,12 @@
 
 Bar: per token, max |y_gpu - y_oracle| <= 4e-3 and cosine >= 0.99999 for
 unit-scale inputs (x ~ N(0,1), W ~ N(0, 0.05^2)). The BF16 intermediate h is
-also compared: a code may differ from the oracle's only where the FP32 and the
-exact value of silu(g)*u fall on different sides of a BF16 rounding boundary,
-i.e. by one BF16 step, and rarely.
+also compared. The kernel rounds silu(g)*u from FP32-accumulated g and u (the
+pages keep accumulators in FP32), the oracle from exact ones, so a code may
+differ by one BF16 step where the two values straddle a rounding boundary, and
+by the FP32 accumulation error where the dot product cancels: at most about
+30 * 2^-24 * sum|x*w| ~ 1e-4 absolute for H <= 4096 at unit scale. Codes must
+agree in all but a small fraction of places.
 """
 import numpy as np
 import pytest
@@ -43,14 +46,18 @@ def _bf16_vals(bits):
     return workload.bf16_bits_to_f32(bits).astype(np.float64)
 
 
+H_ABS = 2e-4  # FP32 accumulation error of g, u carried through silu(g)*u
+
+
 def _check_h(h_gpu, h_ref, max_frac=0.01):
     diff = h_gpu != h_ref
     frac = float(diff.mean()) if diff.size else 0.0
     assert frac <= max_frac, f"{frac:.4%} of intermediate codes differ"
     if diff.any():
         vg, vr = _bf16_vals(h_gpu[diff]), _bf16_vals(h_ref[diff])
-        step = 2.0**-7 * np.maximum(np.abs(vg), np.abs(vr)) + 1e-37
-        assert np.all(np.abs(vg - vr) <= step), "an intermediate differs by more than one BF16 step"
+        allowed = 2.0**-7 * np.maximum(np.abs(vg), np.abs(vr)) + H_ABS
+        worst = float(np.max(np.abs(vg - vr) - allowed))
+        assert worst <= 0, f"an intermediate differs beyond one BF16 step + {H_ABS} (by {worst:.3e})"
 
 
 def _check_y(y_gpu, y_ref):
