@@ -9,8 +9,8 @@
  * kernels:
  *   moe_gate_up : one warp per (token, routed expert, intermediate neuron);
  *                 gate and up dot products share one read of the BF16
- *                 activation, MXFP8 weights are decoded to FP32 on the fly,
- *                 SiLU(gate)*up is written out as BF16.
+ *                 activation, MXFP8 weights are decoded exactly on the fly
+ *                 and accumulated in FP32, SiLU(gate)*up is written as BF16.
  *   moe_down    : one warp per (token, output dim); one FP32 accumulator is
  *                 streamed over all top-k experts' down rows with the routing
  *                 weight folded in, then reduced across the 32 lanes by a
@@ -26,8 +26,9 @@
  * Conventions for every entry point:
  *  - Shapes: H % 32 == 0, I % 32 == 0, E >= 1, 1 <= top_k <= E, B >= 0.
  *    B == 0 is a valid empty batch: nothing is launched, MOE_OK is returned.
- *  - Device pointers: caller-owned (e.g. torch allocations). Weight, x and h
- *    pointers must be 16-byte aligned; ids, w and y 4-byte aligned.
+ *  - Device pointers: caller-owned (e.g. torch allocations). The two code
+ *    arrays (gu_codes, d_codes) must be 32-byte aligned, x and h 16-byte
+ *    aligned, ids, w and y 4-byte aligned.
  *  - The library allocates no device memory, never synchronises, and enqueues
  *    its work on `stream` (a cudaStream_t; NULL = the legacy default stream).
  *  - Host-detectable problems (null pointer, bad shape, misalignment) return

@@ -4,25 +4,35 @@
 // Method: "Better MoE model inference with warp decode" (Key claims
 // [§Reorganized parallelism], [§How the two kernels work], [§Warp Independence];
 // Method) and the sd114.wiki "Warp Decode" page (section
-// 技术原理：两个 Kernel 搞定一切): every warp owns one output scalar, streams the
-// weight rows it needs from global memory into a private FP32 accumulator, and
-// finishes with a __shfl_xor_sync butterfly -- no shared memory, no barriers,
-// no cross-warp communication.
+// 技术原理：两个 Kernel 搞定一切): every warp owns output scalars, streams the
+// weight rows it needs from HBM into private FP32 accumulators, and finishes
+// with a __shfl_xor_sync butterfly; no cross-warp reduction exists.
 //
-// GB300 design:
-//  * Each lane owns 16-byte chunks (16 E4M3 codes) of the rows, chunk c of a
-//    warp's stream at lane c % 32, so every warp-wide load instruction reads
-//    512 contiguous bytes. All of a round's loads are issued before any of
-//    them is consumed, to keep bytes in flight (HBM3e latency x bandwidth).
-//  * Weights are read with ld.global.nc + L1::no_allocate (streamed once per
-//    warp; reuse across tokens happens in the 126 MB L2); activations use the
-//    default cached path (the 8 warps of a CTA share them through L1).
-//  * Grid order puts the neuron/output block on the slow axis and the
-//    (token, slot) on the fast axis, so tokens routed to the same expert read
-//    the same rows close together in time and the re-reads hit L2.
-//  * MXFP8 decode: each E8M0 scale is applied once per 16-element partial sum
-//    (an exact power-of-two scaling); E4M3 codes are converted with the
-//    hardware e4m3x2 -> f16x2 conversion, which is exact.
+// GB300 design (numbers from measurements on this part):
+//  * Instruction budget. FP32 FFMA and the mixed-precision fma.rn.f32.f16 issue
+//    at full rate, while every integer, logic and conversion instruction
+//    (LOP3, SHF, PRMT, cvt) issues at half rate. The inner loop is therefore
+//      hardware cvt e4m3x2 -> f16x2        (0.5 half-rate instr / weight)
+//      fma.rn.f32.f16 activation x weight  (1 full-rate instr / weight)
+//    The product of an f16 activation and an E4M3 weight is exact and is
+//    accumulated in FP32, as in the pages' FP32-accumulator design.
+//  * Activations as f16. The BF16 activation row (x for gate/up, the routed
+//    intermediate for down) is converted once per CTA into shared memory as
+//    f16 after a power-of-two scale 2^sigma that puts its largest magnitude in
+//    [2^14, 2^15); results are multiplied back by 2^-sigma. Every BF16 value
+//    within 2^29 of the row's maximum is represented exactly; smaller ones are
+//    rounded to a multiple of 2^-24 * 2^-sigma (far below FP32 accumulation
+//    error). The f16 copy is laid out [4][blocks][16 B] so that 32 lanes
+//    reading 16 B each hit 32 distinct banks.
+//  * Memory. Each lane owns whole 32-element MXFP8 blocks (one E8M0 scale per
+//    block): one 256-bit load of 32 codes per block, so a warp-wide load reads
+//    1 KB of one row contiguously. Weight loads bypass L1 allocation; reuse of
+//    a row by several tokens happens in L2, which the grid order makes likely
+//    (neuron/output block is the slow grid axis, tokens the fast one).
+//  * Latency. moe_gate_up warps loop over several routed slots of one token and
+//    prefetch the next unit's rows into registers while computing the current
+//    one, so each warp keeps HBM requests in flight; moe_down warps own several
+//    outputs that share one read of the intermediate from shared memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -36,23 +46,31 @@ namespace {
 
 constexpr int kWarpsPerCta = 8;  // 8 warps per CTA, as the pages give for moe_gate_up
 constexpr int kThreads = kWarpsPerCta * 32;
-constexpr int kRound = 4;  // 16-byte chunks per lane per load round
+constexpr int kSegBlocksPerLane = 2;               // gate/up: 32-element blocks per lane per unit
+constexpr int kSegBlocks = 32 * kSegBlocksPerLane;  // blocks of one row per unit (2048 elements)
+constexpr int kMinCtas = 8 * 152;                  // enough CTAs to fill 152 SMs several times
 
 // ---------------------------------------------------------------- loads ----
 
-__device__ __forceinline__ uint4 ld_stream16(const void* p) {
-  uint4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
+struct Codes32 {
+  uint32_t w[8];  // 32 E4M3 codes, element 4i+b in byte b of w[i]
+};
+
+// One 32-element block of codes: a 256-bit load that does not allocate in L1.
+__device__ __forceinline__ Codes32 ld_codes32(const uint8_t* p) {
+  Codes32 c;
+  asm("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(c.w[0]), "=r"(c.w[1]), "=r"(c.w[2]), "=r"(c.w[3]), "=r"(c.w[4]), "=r"(c.w[5]),
+        "=r"(c.w[6]), "=r"(c.w[7])
+      : "l"(p));
+  return c;
 }
 
 __device__ __forceinline__ uint4 ld_cached16(const void* p) {
   uint4 r;
   asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
   return r;
 }
 
@@ -66,42 +84,86 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
   return __uint_as_float(bits);
 }
 
-// Two E4M3 codes (low byte = first element) -> two FP32 values, exact.
-__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
-  uint32_t h2;
-  const unsigned short in = (unsigned short)two_codes;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
-  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+// 2^e for e in [-126, 127], exact.
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// Four E4M3 codes (one word) -> two f16x2 words, exact (hardware conversion).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{.reg .b16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
-// BF16 pair (low half = first element) -> FP32, exact widening.
+// c + a.lo*b.lo + a.hi*b.hi with f16 operands, exact products, FP32 sums.
+__device__ __forceinline__ float fma2_f16(uint32_t a, uint32_t b, float c) {
+  asm("{.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %1;\n\t"
+      "mov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
+      "fma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+      : "+f"(c)
+      : "r"(a), "r"(b));
+  return c;
+}
+
+// sum over one 32-element block: f16 activations a[16 words] x E4M3 codes.
+__device__ __forceinline__ float block_dot(const uint32_t (&a)[16], const Codes32& c) {
+  float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t lo, hi;
+    e4m3x4_to_f16x4(c.w[i], lo, hi);
+    s0 = fma2_f16(a[2 * i], lo, s0);
+    s1 = fma2_f16(a[2 * i + 1], hi, s1);
+  }
+  return s0 + s1;
+}
+
+// 16 f16 activations of block b from the swizzled shared copy ([4][nblk] x 16 B).
+__device__ __forceinline__ void ld_act_block(const uint4* act, int nblk, int b, uint32_t (&a)[16]) {
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint4 v = act[m * nblk + b];
+    a[4 * m + 0] = v.x;
+    a[4 * m + 1] = v.y;
+    a[4 * m + 2] = v.z;
+    a[4 * m + 3] = v.w;
+  }
+}
+
+// ------------------------------------------------------- activation prologue
+// BF16 row(s) in global memory -> f16 x 2^sigma in shared memory, sigma chosen
+// per row group so that the largest magnitude lands in [2^14, 2^15).
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// 16 activations (two 16-byte chunks of BF16) -> FP32 registers.
-__device__ __forceinline__ void widen16(const uint4& a, const uint4& b, float (&f)[16]) {
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+__device__ __forceinline__ float absmax8(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float m = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    f[2 * i] = bf16_lo(w[i]);
-    f[2 * i + 1] = bf16_hi(w[i]);
-  }
+  for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+  return m;
 }
 
-// sum_i f[i] * e4m3(code_i) over one 16-byte chunk of codes.
-__device__ __forceinline__ float dot16(const uint4& codes, const float (&f)[16]) {
-  const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
-  float acc = 0.0f;
+__device__ __forceinline__ uint4 to_f16x8(const uint4& v, float scale) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 lo = e4m3x2_to_f32x2(w[i]);
-    const float2 hi = e4m3x2_to_f32x2(w[i] >> 16);
-    acc = fmaf(f[4 * i + 0], lo.x, acc);
-    acc = fmaf(f[4 * i + 1], lo.y, acc);
-    acc = fmaf(f[4 * i + 2], hi.x, acc);
-    acc = fmaf(f[4 * i + 3], hi.y, acc);
+    const __half2 h = __floats2half2_rn(bf16_lo(w[i]) * scale, bf16_hi(w[i]) * scale);
+    o[i] = *reinterpret_cast<const uint32_t*>(&h);
   }
-  return acc;
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, m));
+  return v;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -110,139 +172,258 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// sigma such that m * 2^sigma is in [2^14, 2^15); 0 for m = 0, inf or NaN.
+__device__ __forceinline__ int pow2_shift_for(float m) {
+  if (!(m > 0.0f) || isinf(m)) return 0;
+  int ex;
+  frexpf(m, &ex);  // m = f * 2^ex, f in [0.5, 1)
+  return min(126, max(-126, 15 - ex));
+}
+
+// Convert `rows` BF16 rows of `len` elements (row r at src + r*len) into the
+// swizzled f16 layout dst[r][4][len/32] (uint4 units) with one shared scale.
+// Returns sigma. Must be called by all threads of the CTA.
+__device__ int stage_activations(const uint16_t* __restrict__ src, int rows, int len,
+                                 uint4* dst, float* red) {
+  const int pieces_per_row = len >> 3;  // 16-byte pieces (8 elements)
+  const int pieces = rows * pieces_per_row;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  float m = 0.0f;
+  for (int p = threadIdx.x; p < pieces; p += kThreads) m = fmaxf(m, absmax8(ld_cached16(s4 + p)));
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = red[0];
+#pragma unroll
+  for (int i = 1; i < kWarpsPerCta; ++i) m = fmaxf(m, red[i]);
+  const int sigma = pow2_shift_for(m);
+  const float up = exp2i(sigma);
+  const int nblk = len >> 5;
+  for (int p = threadIdx.x; p < pieces; p += kThreads) {
+    const int r = p / pieces_per_row, q = p - r * pieces_per_row;
+    dst[r * pieces_per_row + (q & 3) * nblk + (q >> 2)] = to_f16x8(ld_cached16(s4 + p), up);
+  }
+  __syncthreads();
+  return sigma;
+}
+
 __device__ __forceinline__ void flag_invalid(int32_t* err) {
   if (err) atomicOr(err, 1);
 }
 
 // ------------------------------------------------------------ moe_gate_up --
-// grid = (B*top_k pairs, ceil(I / 8)); block = 8 warps; warp w of block
-// (p, nb) computes neuron n = 8*nb + w of pair p = t*top_k + j.
-__global__ void __launch_bounds__(kThreads)
+// grid.x = B * ceil(top_k / SPW) (token, slot group), grid.y = I / 8 (neuron
+// block); 8 warps, warp w computes neuron n = 8*blockIdx.y + w for the SPW
+// routed slots of its group. Dynamic shared memory: H f16 (the scaled x row).
+//
+// A warp's work is a sequence of units (slot, segment of 2048 row elements);
+// the gate and up codes of unit u+1 are loaded while unit u is computed.
+
+struct GateUpUnit {
+  Codes32 g[kSegBlocksPerLane], u[kSegBlocksPerLane];
+  uint32_t sg[kSegBlocksPerLane], su[kSegBlocksPerLane];
+};
+
+template <int SPW>
+__global__ void __launch_bounds__(kThreads, 2)
     moe_gate_up_kernel(const uint8_t* __restrict__ gu_codes,
                        const uint8_t* __restrict__ gu_scales,
                        const uint16_t* __restrict__ x, const int32_t* __restrict__ ids,
                        uint16_t* __restrict__ h, int32_t* __restrict__ err, int H, int I,
                        int E, int top_k) {
+  extern __shared__ uint4 xs[];
+  __shared__ float red[kWarpsPerCta];
   const int lane = threadIdx.x & 31;
-  const int p = blockIdx.x;
+  const int groups = (top_k + SPW - 1) / SPW;
+  const int t = blockIdx.x / groups;
+  const int j0 = (blockIdx.x - t * groups) * SPW;
   const int n = blockIdx.y * kWarpsPerCta + (threadIdx.x >> 5);
-  if (n >= I) return;
-  const int t = p / top_k;
-  const int e = __ldg(ids + p);
-  if (e < 0 || e >= E) {
-    if (lane == 0) {
-      h[(size_t)p * I + n] = 0;
-      flag_invalid(err);
+  const int nblk = H >> 5;
+
+  const int sigma = stage_activations(x + (size_t)t * H, 1, H, xs, red);
+  const float unscale = exp2i(-sigma);
+
+  const int nslots = min(SPW, top_k - j0);
+  const int nseg = (nblk + kSegBlocks - 1) / kSegBlocks;
+  const int units = nslots * nseg;
+
+  // expert id of slot s of this group (uniform across the warp; an L1 hit)
+  auto expert = [&](int s) { return __ldg(ids + (size_t)t * top_k + j0 + s); };
+
+  auto load_unit = [&](int uidx, GateUpUnit& U) {
+    const int s = uidx / nseg, seg = uidx - s * nseg;
+    const int e = expert(s);
+    if (e < 0 || e >= E) return;
+    const size_t row = (size_t)e * I + n;
+    const uint8_t* gc = gu_codes + row * 2 * (size_t)H;
+    const uint8_t* sc = gu_scales + row * 2 * (size_t)nblk;
+#pragma unroll
+    for (int q = 0; q < kSegBlocksPerLane; ++q) {
+      const int b = seg * kSegBlocks + q * 32 + lane;
+      if (b < nblk) {
+        U.g[q] = ld_codes32(gc + (size_t)b * 32);
+        U.u[q] = ld_codes32(gc + H + (size_t)b * 32);
+        U.sg[q] = __ldg(sc + b);
+        U.su[q] = __ldg(sc + nblk + b);
+      }
     }
-    return;
-  }
-  const int chunks = H >> 4;   // 16-byte chunks per row
-  const int blocks = H >> 5;   // scales per row
-  const uint8_t* grow = gu_codes + ((size_t)e * I + n) * 2 * (size_t)H;  // up row at +H
-  const uint8_t* srow = gu_scales + ((size_t)e * I + n) * 2 * (size_t)blocks;
-  const uint16_t* xrow = x + (size_t)t * H;
+  };
 
   float g = 0.0f, u = 0.0f;
-  for (int c0 = 0; c0 < chunks; c0 += 32 * kRound) {
-    uint4 gw[kRound], uw[kRound], xa[kRound], xb[kRound];
-    uint32_t gs[kRound], us[kRound];
+  auto compute_unit = [&](int uidx, const GateUpUnit& U) {
+    const int s = uidx / nseg, seg = uidx - s * nseg;
+    const int e = expert(s);
+    const bool ok = e >= 0 && e < E;
+    if (ok) {
 #pragma unroll
-    for (int q = 0; q < kRound; ++q) {
-      const int c = c0 + q * 32 + lane;
-      if (c < chunks) {
-        gw[q] = ld_stream16(grow + (size_t)c * 16);
-        uw[q] = ld_stream16(grow + H + (size_t)c * 16);
-        xa[q] = ld_cached16(xrow + c * 16);
-        xb[q] = ld_cached16(xrow + c * 16 + 8);
-        gs[q] = __ldg(srow + (c >> 1));
-        us[q] = __ldg(srow + blocks + (c >> 1));
+      for (int q = 0; q < kSegBlocksPerLane; ++q) {
+        const int b = seg * kSegBlocks + q * 32 + lane;
+        if (b < nblk) {
+          uint32_t a[16];
+          ld_act_block(xs, nblk, b, a);
+          g = fmaf(block_dot(a, U.g[q]), e8m0_to_f32(U.sg[q]), g);
+          u = fmaf(block_dot(a, U.u[q]), e8m0_to_f32(U.su[q]), u);
+        }
       }
     }
-#pragma unroll
-    for (int q = 0; q < kRound; ++q) {
-      const int c = c0 + q * 32 + lane;
-      if (c < chunks) {
-        float xf[16];
-        widen16(xa[q], xb[q], xf);
-        g = fmaf(dot16(gw[q], xf), e8m0_to_f32(gs[q]), g);
-        u = fmaf(dot16(uw[q], xf), e8m0_to_f32(us[q]), u);
+    if (seg == nseg - 1) {  // last segment of this slot: finish the neuron
+      const size_t out = ((size_t)t * top_k + j0 + s) * I + n;
+      if (ok) {
+        g = warp_sum(g) * unscale;
+        u = warp_sum(u) * unscale;
+        if (lane == 0) {
+          const float sl = g / (1.0f + expf(-g));
+          const __nv_bfloat16 hv = __float2bfloat16_rn(sl * u);
+          h[out] = *reinterpret_cast<const uint16_t*>(&hv);
+        }
+      } else if (lane == 0) {
+        h[out] = 0;
+        flag_invalid(err);
       }
+      g = 0.0f;
+      u = 0.0f;
     }
-  }
-  g = warp_sum(g);
-  u = warp_sum(u);
-  if (lane == 0) {
-    const float s = g / (1.0f + expf(-g));
-    const __nv_bfloat16 hv = __float2bfloat16_rn(s * u);
-    h[(size_t)p * I + n] = *reinterpret_cast<const uint16_t*>(&hv);
+  };
+
+  GateUpUnit A, B;
+  if (units > 0) load_unit(0, A);
+  for (int uidx = 0; uidx < units; uidx += 2) {
+    if (uidx + 1 < units) load_unit(uidx + 1, B);
+    compute_unit(uidx, A);
+    if (uidx + 1 >= units) break;
+    if (uidx + 2 < units) load_unit(uidx + 2, A);
+    compute_unit(uidx + 1, B);
   }
 }
 
 // --------------------------------------------------------------- moe_down --
-// grid = (B tokens, ceil(H / 8)); block = 8 warps; warp w of block (t, ob)
-// computes output o = 8*ob + w of token t. The top_k down rows form one flat
-// stream of top_k * I/16 chunks spread over the lanes; every chunk adds
-// (partial dot) * scale * routing weight into the lane's single accumulator.
-__global__ void __launch_bounds__(kThreads)
+// grid.x = B (token), grid.y = H / (8*OPW) (output block); 8 warps, warp w owns
+// outputs o0 .. o0+OPW-1 with o0 = (8*blockIdx.y + w) * OPW. Dynamic shared
+// memory: the token's top_k intermediates as scaled f16 (top_k * I), plus
+// the token's ids and routing weights.
+//
+// A warp's top_k * I/32 (slot, block) units are spread over its lanes; every
+// unit multiplies one block of the intermediate (read once from shared memory)
+// with the same block of the OPW down rows, and adds partial * scale * w[slot]
+// into the lane's OPW FP32 accumulators -- the routing weight is folded into
+// the sum, so no per-expert output exists.
+
+template <int OPW>
+struct DownUnit {
+  Codes32 c[OPW];
+  uint32_t s[OPW];
+};
+
+template <int OPW>
+__global__ void __launch_bounds__(kThreads, 2)
     moe_down_kernel(const uint8_t* __restrict__ d_codes, const uint8_t* __restrict__ d_scales,
                     const uint16_t* __restrict__ h, const int32_t* __restrict__ ids,
                     const float* __restrict__ wts, float* __restrict__ y,
                     int32_t* __restrict__ err, int H, int I, int E, int top_k) {
+  extern __shared__ uint4 dyn[];
+  __shared__ float red[kWarpsPerCta];
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x;
-  const int o = blockIdx.y * kWarpsPerCta + (threadIdx.x >> 5);
-  if (o >= H) return;
-  const int chunks = I >> 4;  // per down row
-  const int blocks = I >> 5;
-  const int total = top_k * chunks;
-  // (slot, chunk-in-row) of this lane's first chunk; advanced by 32 per step
-  int j = lane / chunks;
-  int r = lane - j * chunks;
+  const int o0 = (blockIdx.y * kWarpsPerCta + (threadIdx.x >> 5)) * OPW;
+  const int nblk = I >> 5;
+  uint4* hs = dyn;                                                      // top_k*I/8 uint4
+  int* s_ids = reinterpret_cast<int*>(dyn + (size_t)top_k * (I >> 3));  // top_k
+  float* s_w = reinterpret_cast<float*>(s_ids + top_k);                 // top_k
+
+  for (int j = threadIdx.x; j < top_k; j += kThreads) {
+    s_ids[j] = __ldg(ids + (size_t)t * top_k + j);
+    s_w[j] = __ldg(wts + (size_t)t * top_k + j);
+  }
+  const int sigma = stage_activations(h + (size_t)t * top_k * I, top_k, I, hs, red);
+  const float unscale = exp2i(-sigma);
+
+  const int units = top_k * nblk;
+  float acc[OPW];
+#pragma unroll
+  for (int r = 0; r < OPW; ++r) acc[r] = 0.0f;
   bool bad = false;
 
-  float acc = 0.0f;
-  for (int f0 = 0; f0 < total; f0 += 32 * kRound) {
-    uint4 cw[kRound], ha[kRound], hb[kRound];
-    uint32_t sc[kRound];
-    float wj[kRound];
-    bool live[kRound];
+  auto load_unit = [&](int jj, int bb, DownUnit<OPW>& U) {
+    const int e = s_ids[jj];
+    if (e < 0 || e >= E) return;
 #pragma unroll
-    for (int q = 0; q < kRound; ++q) {
-      const int f = f0 + q * 32 + lane;
-      live[q] = false;
-      if (f < total) {
-        const int slot = t * top_k + j;
-        const int e = __ldg(ids + slot);
-        if (e >= 0 && e < E) {
-          const size_t row = (size_t)e * H + o;
-          cw[q] = ld_stream16(d_codes + row * I + (size_t)r * 16);
-          sc[q] = __ldg(d_scales + row * blocks + (r >> 1));
-          ha[q] = ld_cached16(h + (size_t)slot * I + r * 16);
-          hb[q] = ld_cached16(h + (size_t)slot * I + r * 16 + 8);
-          wj[q] = __ldg(wts + slot);
-          live[q] = true;
-        } else {
-          bad = true;
-        }
-        r += 32;
-        while (r >= chunks) {
-          r -= chunks;
-          ++j;
-        }
-      }
+    for (int r = 0; r < OPW; ++r) {
+      const size_t row = (size_t)e * H + o0 + r;
+      U.c[r] = ld_codes32(d_codes + row * I + (size_t)bb * 32);
+      U.s[r] = __ldg(d_scales + row * nblk + bb);
     }
+  };
+  auto compute_unit = [&](int jj, int bb, const DownUnit<OPW>& U) {
+    const int e = s_ids[jj];
+    if (e < 0 || e >= E) {
+      bad = true;
+      return;
+    }
+    const float wj = s_w[jj];
+    uint32_t a[16];
+    ld_act_block(hs + (size_t)jj * (I >> 3), nblk, bb, a);
 #pragma unroll
-    for (int q = 0; q < kRound; ++q) {
-      if (live[q]) {
-        float hf[16];
-        widen16(ha[q], hb[q], hf);
-        acc = fmaf(dot16(cw[q], hf), e8m0_to_f32(sc[q]) * wj[q], acc);
-      }
+    for (int r = 0; r < OPW; ++r)
+      acc[r] = fmaf(block_dot(a, U.c[r]), e8m0_to_f32(U.s[r]) * wj, acc[r]);
+  };
+  // (slot, block) of a unit, advanced by 32 units (one lane stride)
+  auto advance = [&](int& jj, int& bb) {
+    bb += 32;
+    while (bb >= nblk) {
+      bb -= nblk;
+      ++jj;
     }
+  };
+
+  DownUnit<OPW> A, B;
+  int ja = lane / nblk, ba = lane - (lane / nblk) * nblk;  // this lane's first unit
+  int u0 = lane;
+  if (u0 < units) load_unit(ja, ba, A);
+  while (u0 < units) {
+    int jb = ja, bbv = ba;
+    advance(jb, bbv);
+    const bool has_b = u0 + 32 < units;
+    if (has_b) load_unit(jb, bbv, B);
+    compute_unit(ja, ba, A);
+    if (!has_b) break;
+    int jc = jb, bc = bbv;
+    advance(jc, bc);
+    const bool has_c = u0 + 64 < units;
+    if (has_c) load_unit(jc, bc, A);
+    compute_unit(jb, bbv, B);
+    ja = jc;
+    ba = bc;
+    u0 += 64;
   }
-  acc = warp_sum(acc);
+#pragma unroll
+  for (int r = 0; r < OPW; ++r) acc[r] = warp_sum(acc[r]) * unscale;
   if (bad) flag_invalid(err);
-  if (lane == 0) y[(size_t)t * H + o] = acc;
+  if (lane < OPW) {
+    float v = acc[0];
+#pragma unroll
+    for (int r = 1; r < OPW; ++r) v = (lane == r) ? acc[r] : v;
+    y[(size_t)t * H + o0 + lane] = v;
+  }
 }
 
 // ------------------------------------------------------------- host side ---
@@ -277,12 +458,81 @@ moe_status check_weights(const moe_weights* w, bool gate_up, bool down) {
   if (!w) return MOE_ERR_NULL;
   if ((gate_up && (!w->gu_codes || !w->gu_scales)) || (down && (!w->d_codes || !w->d_scales)))
     return MOE_ERR_NULL;
-  if ((gate_up && !aligned(w->gu_codes, 16)) || (down && !aligned(w->d_codes, 16))) {
-    set_error_msg("alignment: weight codes must be 16-byte aligned");
+  if ((gate_up && !aligned(w->gu_codes, 32)) || (down && !aligned(w->d_codes, 32))) {
+    set_error_msg("alignment: weight codes must be 32-byte aligned");
     return MOE_ERR_ALIGN;
   }
   return MOE_OK;
 }
+
+constexpr size_t kMaxDynSmem = 227 * 1024;
+
+// Opt a kernel into more than the default 48 KB of dynamic shared memory.
+template <typename K>
+moe_status allow_smem(K kernel, size_t bytes) {
+  if (bytes > kMaxDynSmem) {
+    set_error_msg("shape: activation row does not fit in shared memory");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (bytes > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) {
+      set_error("cudaFuncSetAttribute", e);
+      return MOE_ERR_CUDA;
+    }
+  }
+  return MOE_OK;
+}
+
+// Slots per warp of moe_gate_up: as many as keep at least kMinCtas CTAs.
+int pick_spw(int B, int top_k, int I) {
+  const int spws[4] = {8, 4, 2, 1};
+  for (int v : spws) {
+    if (v > top_k) continue;
+    const int64_t ctas = (int64_t)B * ((top_k + v - 1) / v) * (I / kWarpsPerCta);
+    if (ctas >= kMinCtas) return v;
+  }
+  return 1;
+}
+
+// Outputs per warp of moe_down: as many as keep at least kMinCtas CTAs.
+int pick_opw(int B, int H) {
+  const int opws[3] = {4, 2, 1};
+  for (int v : opws) {
+    const int64_t ctas = (int64_t)B * (H / (kWarpsPerCta * v));
+    if (ctas >= kMinCtas) return v;
+  }
+  return 1;
+}
+
+template <int SPW>
+moe_status launch_gate_up(const moe_shape* s, const moe_weights* w, const uint16_t* x,
+                          const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
+                          cudaStream_t st) {
+  const size_t smem = (size_t)s->H * 2;
+  moe_status rc = allow_smem(moe_gate_up_kernel<SPW>, smem);
+  if (rc != MOE_OK) return rc;
+  const int groups = (s->top_k + SPW - 1) / SPW;
+  const dim3 grid((unsigned)(B * groups), (unsigned)(s->I / kWarpsPerCta));
+  moe_gate_up_kernel<SPW><<<grid, kThreads, smem, st>>>(w->gu_codes, w->gu_scales, x, ids, h,
+                                                        err, s->H, s->I, s->E, s->top_k);
+  return MOE_OK;
+}
+
+template <int OPW>
+moe_status launch_down(const moe_shape* s, const moe_weights* w, const uint16_t* h,
+                       const int32_t* ids, const float* wts, int32_t B, float* y, int32_t* err,
+                       cudaStream_t st) {
+  const size_t smem = (size_t)s->top_k * s->I * 2 + (size_t)s->top_k * 8;
+  moe_status rc = allow_smem(moe_down_kernel<OPW>, smem);
+  if (rc != MOE_OK) return rc;
+  const dim3 grid((unsigned)B, (unsigned)(s->H / (kWarpsPerCta * OPW)));
+  moe_down_kernel<OPW><<<grid, kThreads, smem, st>>>(w->d_codes, w->d_scales, h, ids, wts, y,
+                                                     err, s->H, s->I, s->E, s->top_k);
+  return MOE_OK;
+}
+
 
 moe_status launch_status(const char* what) {
   const cudaError_t e = cudaGetLastError();
@@ -305,9 +555,13 @@ moe_status gate_up_impl(const moe_shape* s, const moe_weights* w, const uint16_t
     set_error_msg("alignment: x and h need 16 bytes, ids and err_flag 4");
     return MOE_ERR_ALIGN;
   }
-  const dim3 grid((unsigned)(B * s->top_k), (unsigned)((s->I + kWarpsPerCta - 1) / kWarpsPerCta));
-  moe_gate_up_kernel<<<grid, kThreads, 0, st>>>(w->gu_codes, w->gu_scales, x, ids, h, err, s->H,
-                                                s->I, s->E, s->top_k);
+  switch (pick_spw(B, s->top_k, s->I)) {
+    case 8: rc = launch_gate_up<8>(s, w, x, ids, B, h, err, st); break;
+    case 4: rc = launch_gate_up<4>(s, w, x, ids, B, h, err, st); break;
+    case 2: rc = launch_gate_up<2>(s, w, x, ids, B, h, err, st); break;
+    default: rc = launch_gate_up<1>(s, w, x, ids, B, h, err, st); break;
+  }
+  if (rc != MOE_OK) return rc;
   return launch_status("moe_gate_up launch");
 }
 
@@ -324,10 +578,12 @@ moe_status down_impl(const moe_shape* s, const moe_weights* w, const uint16_t* h
     set_error_msg("alignment: h needs 16 bytes, ids/wts/y/err_flag 4");
     return MOE_ERR_ALIGN;
   }
-  if ((unsigned)B > 0x7FFFFFFFu) return MOE_ERR_SHAPE;
-  const dim3 grid((unsigned)B, (unsigned)((s->H + kWarpsPerCta - 1) / kWarpsPerCta));
-  moe_down_kernel<<<grid, kThreads, 0, st>>>(w->d_codes, w->d_scales, h, ids, wts, y, err, s->H,
-                                             s->I, s->E, s->top_k);
+  switch (pick_opw(B, s->H)) {
+    case 4: rc = launch_down<4>(s, w, h, ids, wts, B, y, err, st); break;
+    case 2: rc = launch_down<2>(s, w, h, ids, wts, B, y, err, st); break;
+    default: rc = launch_down<1>(s, w, h, ids, wts, B, y, err, st); break;
+  }
+  if (rc != MOE_OK) return rc;
   return launch_status("moe_down launch");
 }
 

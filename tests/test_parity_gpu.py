@@ -158,6 +158,30 @@ def test_ragged_and_small_shapes(H, I, E, k, B):
     _check_h(h, h_ref)
 
 
+def test_activation_scale_extremes(q30):
+    """Tokens whose activations are far from unit scale or span a wide range.
+
+    The kernels hold activations as f16 times a per-row power of two; results
+    must still match the oracle relative to the output's own scale.
+    """
+    B = 4
+    x, ids, w = workload.tokens(q30.shape, B, batch=77)
+    xf = workload.bf16_bits_to_f32(x).copy()
+    xf[0] *= 1e8
+    xf[1] *= 1e-8
+    xf[2, ::2] *= 1e4          # half the row large, half small: range ~1e8
+    xf[2, 1::2] *= 1e-4
+    xf[3, :8] = [3e-9, -7e-10, 65504.0, 70000.0, -1e5, 2.0**-14, 2.0**-24, 0.0]
+    xb = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    y, h = _run_layer(q30, xb, ids, w)
+    y_ref, h_ref, _ = oracle.moe_layer(q30.ref, xb, ids, w, return_h=True)
+    for t in range(B):
+        scale = float(np.max(np.abs(y_ref[t])))
+        assert scale > 0 and np.all(np.isfinite(y[t]))
+        d, cos = parity_stats(y[t:t + 1] / scale, y_ref[t:t + 1] / scale)
+        assert d <= 1e-4 and cos >= MIN_COS, (t, d, cos)
+
+
 def test_duplicate_ids_and_all_tokens_on_one_expert(tiny):
     B = 16
     x, _, _ = workload.tokens(tiny.shape, B, batch=5)
