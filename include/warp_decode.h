@@ -149,6 +149,29 @@ moe_status moe_layer_host(const moe_shape* shape, const moe_weights* w, const ui
                           uint16_t* x_dev, int32_t* ids_dev, float* wts_dev, uint16_t* h_dev,
                           float* y_dev, float* y_host, int32_t* err_flag, void* stream);
 
+/*
+ * moe_layer_noalloc -- the whole layer (as moe_layer) for callers that cannot
+ * allocate device memory: code that runs inside a host framework which owns
+ * every device allocation through its own pool, or a latency-critical decode
+ * loop that must not call cudaMalloc (it can synchronise the device). The
+ * pages have no counterpart to this entry point.
+ *   The intermediate lives in an array inside this library, of at most
+ *   MOE_NOALLOC_MAX_INTERMEDIATE BF16 values (2 MiB) on every GPU that calls
+ *   it, held until the library is unloaded. B * top_k * I above that limit
+ *   returns MOE_ERR_SHAPE (moe_last_error() says why) before anything runs.
+ *   The first call on each device looks up the array's device address with
+ *   cudaGetSymbolAddress, with that device current; make that first call
+ *   before any stream capture. The call allocates nothing.
+ *   All calls share the one array: calls whose work overlaps on the GPU (for
+ *   example on two streams at once) race on it. Each call overwrites every
+ *   value it reads, so nothing needs clearing between calls.
+ * Arguments, layouts and error behaviour otherwise as for moe_layer.
+ */
+#define MOE_NOALLOC_MAX_INTERMEDIATE (1u << 20)
+moe_status moe_layer_noalloc(const moe_shape* shape, const moe_weights* w, const uint16_t* x,
+                             const int32_t* ids, const float* wts, int32_t B, float* y,
+                             int32_t* err_flag, void* stream);
+
 /* Static description of a status code. */
 const char* moe_status_string(moe_status status);
 

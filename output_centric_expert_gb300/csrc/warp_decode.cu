@@ -39,6 +39,7 @@
 
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 
 #include "warp_decode.h"
 
@@ -666,3 +667,73 @@ extern "C" const char* moe_status_string(moe_status s) {
 }
 
 extern "C" const char* moe_last_error(void) { return g_last_error; }
+
+// ------------------------------------------ allocation-free layer variant --
+// moe_layer_noalloc: the whole layer with the intermediate kept in a fixed
+// array that belongs to this library instead of a caller-provided buffer, for
+// callers that cannot allocate device memory themselves. The array lives for
+// as long as the library is loaded, on every GPU that uses it.
+
+static __device__ __align__(256) uint16_t g_noalloc_intermediate[MOE_NOALLOC_MAX_INTERMEDIATE];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+uint16_t* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the fixed intermediate array on the current device. Host
+// code must not pass the array's name to a kernel (on the host it only stands
+// for the symbol), so the address is looked up once per device, with that
+// device current, and cached.
+moe_status noalloc_intermediate(uint16_t** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error("moe_layer_noalloc: cudaGetDevice", e);
+    return MOE_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kNoAllocMaxDevices) {
+    set_error_msg("moe_layer_noalloc: device index beyond the supported 64 devices");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_intermediate);
+    if (e != cudaSuccess) {
+      set_error("moe_layer_noalloc: cudaGetSymbolAddress", e);
+      return MOE_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = static_cast<uint16_t*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_layer_noalloc(const moe_shape* shape, const moe_weights* w,
+                                        const uint16_t* x, const int32_t* ids, const float* wts,
+                                        int32_t B, float* y, int32_t* err_flag, void* stream) {
+  moe_status rc = check_shape(shape, B);
+  if (rc != MOE_OK) return rc;
+  if ((rc = check_weights(w, true, true)) != MOE_OK) return rc;
+  if (B == 0) return MOE_OK;
+  if (!x || !ids || !wts || !y) return MOE_ERR_NULL;
+  const size_t need = (size_t)B * (size_t)shape->top_k * (size_t)shape->I;
+  if (need > (size_t)MOE_NOALLOC_MAX_INTERMEDIATE) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "moe_layer_noalloc: B*top_k*I = %zu BF16 values exceeds the fixed intermediate "
+             "capacity of %zu; use moe_layer with a caller-provided buffer",
+             need, (size_t)MOE_NOALLOC_MAX_INTERMEDIATE);
+    return MOE_ERR_SHAPE;
+  }
+  uint16_t* h = nullptr;
+  if ((rc = noalloc_intermediate(&h)) != MOE_OK) return rc;
+  // every intermediate element is written by moe_gate_up (0 for an invalid
+  // id) before moe_down reads it on the same stream: nothing needs clearing
+  rc = gate_up_impl(shape, w, x, ids, B, h, err_flag, (cudaStream_t)stream);
+  if (rc != MOE_OK) return rc;
+  return down_impl(shape, w, h, ids, wts, B, y, err_flag, (cudaStream_t)stream);
+}

@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
         L.moe_down.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp]
         L.moe_layer.restype = ctypes.c_int
         L.moe_layer.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp, vp]
+        L.moe_layer_noalloc.restype = ctypes.c_int
+        L.moe_layer_noalloc.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp]
         L.moe_layer_host.restype = ctypes.c_int
         L.moe_layer_host.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_status_string.restype = ctypes.c_char_p
@@ -197,6 +199,27 @@ def moe_layer(weights: DeviceWeights, x: torch.Tensor, ids: torch.Tensor, wts: t
     return y
 
 
+def moe_layer_noalloc(weights: DeviceWeights, x: torch.Tensor, ids: torch.Tensor,
+                      wts: torch.Tensor, y: torch.Tensor, err_flag: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """The whole layer without a caller-provided intermediate buffer.
+
+    For callers that cannot allocate device memory: the intermediate lives in
+    a fixed array inside the library (at most MOE_NOALLOC_MAX_INTERMEDIATE
+    BF16 values, B * top_k * I), shared by all calls.
+    """
+    B = x.shape[0]
+    _check("moe_layer_noalloc", lib().moe_layer_noalloc(
+        ctypes.byref(weights.shape), ctypes.byref(weights.struct), _ptr(x, _BF16, "x"),
+        _ptr(ids, (torch.int32,), "ids"), _ptr(wts, (torch.float32,), "wts"), B,
+        _ptr(y, (torch.float32,), "y"), _ptr(err_flag, (torch.int32,), "err_flag"),
+        _stream(stream)))
+    return y
+
+
+MOE_NOALLOC_MAX_INTERMEDIATE = 1 << 20
+
+
 def moe_layer_host(weights: DeviceWeights, x_host: torch.Tensor, ids_host: torch.Tensor,
                    wts_host: torch.Tensor, x_dev: torch.Tensor, ids_dev: torch.Tensor,
                    wts_dev: torch.Tensor, h_dev: torch.Tensor, y_dev: torch.Tensor,
@@ -217,4 +240,4 @@ def moe_layer_host(weights: DeviceWeights, x_host: torch.Tensor, ids_host: torch
 def exported_symbols() -> list[str]:
     """The entry points include/warp_decode.h declares."""
     return ["moe_packed_bytes", "moe_pack_weights", "moe_gate_up", "moe_down", "moe_layer",
-            "moe_layer_host", "moe_status_string", "moe_last_error"]
+            "moe_layer_host", "moe_layer_noalloc", "moe_status_string", "moe_last_error"]
