@@ -24,7 +24,8 @@
  * consecutive elements along the reduction axis (H for gate/up, I for down).
  *
  * Conventions for every entry point:
- *  - Shapes: H % 32 == 0, I % 32 == 0, E >= 1, 1 <= top_k <= E, B >= 0.
+ *  - Shapes: H % 32 == 0 and H <= 8192, I % 32 == 0, E >= 1,
+ *    1 <= top_k <= E, B >= 0.
  *    B == 0 is a valid empty batch: nothing is launched, MOE_OK is returned.
  *  - Device pointers: caller-owned (e.g. torch allocations). The two code
  *    arrays (gu_codes, d_codes) must be 32-byte aligned, x and h 16-byte

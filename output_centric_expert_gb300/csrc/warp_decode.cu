@@ -167,12 +167,6 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, m);
-  return v;
-}
-
 // sigma such that m * 2^sigma is in [2^14, 2^15); 0 for m = 0, inf or NaN.
 __device__ __forceinline__ int pow2_shift_for(float m) {
   if (!(m > 0.0f) || isinf(m)) return 0;
@@ -212,20 +206,51 @@ __device__ __forceinline__ void flag_invalid(int32_t* err) {
   if (err) atomicOr(err, 1);
 }
 
+// Sum each of the V (a power of two, <= 32) values of v over the 32 lanes of
+// the warp with one transposing butterfly: at every step a lane keeps half
+// of its values and receives its partner's partial sums of that half, so the
+// values are reduced together in V-1 + (5 - log2 V) shuffles instead of
+// V*5. Afterwards lane l holds the total of value index l >> (5 - log2 V).
+template <int V>
+__device__ __forceinline__ float warp_sum_transposed(float (&v)[V]) {
+  static_assert(V == 1 || V == 2 || V == 4 || V == 8 || V == 16 || V == 32, "V: power of two");
+  constexpr int L = V == 1 ? 0 : V == 2 ? 1 : V == 4 ? 2 : V == 8 ? 3 : V == 16 ? 4 : 5;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < L; ++k) {
+    const int m = 16 >> k;
+    const int half = V >> (k + 1);
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, m);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int m = 16 >> L; m >= 1; m >>= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, m);
+  return r;
+}
+
 // ------------------------------------------------------------ moe_gate_up --
 // grid.x = B * ceil(top_k / SPW) (token, slot group), grid.y = I / 8 (neuron
 // block); 8 warps, warp w computes neuron n = 8*blockIdx.y + w for the SPW
 // routed slots of its group. Dynamic shared memory: H f16 (the scaled x row).
 //
-// A warp's work is a sequence of units (slot, segment of 2048 row elements);
-// the gate and up codes of unit u+1 are loaded while unit u is computed.
+// A warp's work is SPW * NSEG units (slot, segment of 2048 row elements),
+// unrolled at compile time; the gate and up codes of unit u+1 are loaded into
+// registers while unit u is computed. Each lane keeps one (gate, up) partial
+// pair per slot; all of them are reduced together at the end and the SwiGLU
+// epilogue of the SPW neurons runs once, in SPW lanes side by side.
 
 struct GateUpUnit {
   Codes32 g[kSegBlocksPerLane], u[kSegBlocksPerLane];
   uint32_t sg[kSegBlocksPerLane], su[kSegBlocksPerLane];
 };
 
-template <int SPW>
+template <int SPW, int NSEG>
 __global__ void __launch_bounds__(kThreads, 2)
     moe_gate_up_kernel(const uint8_t* __restrict__ gu_codes,
                        const uint8_t* __restrict__ gu_scales,
@@ -240,21 +265,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int j0 = (blockIdx.x - t * groups) * SPW;
   const int n = blockIdx.y * kWarpsPerCta + (threadIdx.x >> 5);
   const int nblk = H >> 5;
+  const int nslots = min(SPW, top_k - j0);
+
+  // lane s < nslots holds the expert id of slot s; -1 marks "no slot"
+  const int e_lane = (lane < nslots) ? __ldg(ids + (size_t)t * top_k + j0 + lane) : -1;
 
   const int sigma = stage_activations(x + (size_t)t * H, 1, H, xs, red);
   const float unscale = exp2i(-sigma);
 
-  const int nslots = min(SPW, top_k - j0);
-  const int nseg = (nblk + kSegBlocks - 1) / kSegBlocks;
-  const int units = nslots * nseg;
-
-  // expert id of slot s of this group (uniform across the warp; an L1 hit)
-  auto expert = [&](int s) { return __ldg(ids + (size_t)t * top_k + j0 + s); };
-
-  auto load_unit = [&](int uidx, GateUpUnit& U) {
-    const int s = uidx / nseg, seg = uidx - s * nseg;
-    const int e = expert(s);
-    if (e < 0 || e >= E) return;
+  auto load_unit = [&](int s, int seg, GateUpUnit& U) {
+    const int e = __shfl_sync(0xFFFFFFFFu, e_lane, s);
+    if (s >= nslots || e < 0 || e >= E) return;
     const size_t row = (size_t)e * I + n;
     const uint8_t* gc = gu_codes + row * 2 * (size_t)H;
     const uint8_t* sc = gu_scales + row * 2 * (size_t)nblk;
@@ -270,50 +291,52 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   };
 
-  float g = 0.0f, u = 0.0f;
-  auto compute_unit = [&](int uidx, const GateUpUnit& U) {
-    const int s = uidx / nseg, seg = uidx - s * nseg;
-    const int e = expert(s);
-    const bool ok = e >= 0 && e < E;
-    if (ok) {
+  float acc[2 * SPW];  // acc[s] gate, acc[SPW + s] up partials of slot s
 #pragma unroll
-      for (int q = 0; q < kSegBlocksPerLane; ++q) {
-        const int b = seg * kSegBlocks + q * 32 + lane;
-        if (b < nblk) {
-          uint32_t a[16];
-          ld_act_block(xs, nblk, b, a);
-          g = fmaf(block_dot(a, U.g[q]), e8m0_to_f32(U.sg[q]), g);
-          u = fmaf(block_dot(a, U.u[q]), e8m0_to_f32(U.su[q]), u);
-        }
+  for (int i = 0; i < 2 * SPW; ++i) acc[i] = 0.0f;
+
+  auto compute_unit = [&](int s, int seg, const GateUpUnit& U) {
+    const int e = __shfl_sync(0xFFFFFFFFu, e_lane, s);
+    if (s >= nslots || e < 0 || e >= E) return;
+#pragma unroll
+    for (int q = 0; q < kSegBlocksPerLane; ++q) {
+      const int b = seg * kSegBlocks + q * 32 + lane;
+      if (b < nblk) {
+        uint32_t a[16];
+        ld_act_block(xs, nblk, b, a);
+        acc[s] = fmaf(block_dot(a, U.g[q]), e8m0_to_f32(U.sg[q]), acc[s]);
+        acc[SPW + s] = fmaf(block_dot(a, U.u[q]), e8m0_to_f32(U.su[q]), acc[SPW + s]);
       }
-    }
-    if (seg == nseg - 1) {  // last segment of this slot: finish the neuron
-      const size_t out = ((size_t)t * top_k + j0 + s) * I + n;
-      if (ok) {
-        g = warp_sum(g) * unscale;
-        u = warp_sum(u) * unscale;
-        if (lane == 0) {
-          const float sl = g / (1.0f + expf(-g));
-          const __nv_bfloat16 hv = __float2bfloat16_rn(sl * u);
-          h[out] = *reinterpret_cast<const uint16_t*>(&hv);
-        }
-      } else if (lane == 0) {
-        h[out] = 0;
-        flag_invalid(err);
-      }
-      g = 0.0f;
-      u = 0.0f;
     }
   };
 
-  GateUpUnit A, B;
-  if (units > 0) load_unit(0, A);
-  for (int uidx = 0; uidx < units; uidx += 2) {
-    if (uidx + 1 < units) load_unit(uidx + 1, B);
-    compute_unit(uidx, A);
-    if (uidx + 1 >= units) break;
-    if (uidx + 2 < units) load_unit(uidx + 2, A);
-    compute_unit(uidx + 1, B);
+  constexpr int kUnits = SPW * NSEG;
+  GateUpUnit buf[2];
+  load_unit(0, 0, buf[0]);
+#pragma unroll
+  for (int u = 0; u < kUnits; ++u) {
+    if (u + 1 < kUnits) load_unit((u + 1) / NSEG, (u + 1) % NSEG, buf[(u + 1) & 1]);
+    compute_unit(u / NSEG, u % NSEG, buf[u & 1]);
+  }
+
+  // lane l now holds the total of value l >> (4 - log2 SPW): gate sums in
+  // lanes 0..15, the matching up sums 16 lanes higher
+  const float tot = warp_sum_transposed<2 * SPW>(acc);
+  const float up_tot = __shfl_down_sync(0xFFFFFFFFu, tot, 16);
+  constexpr int kLanesPerSlot = 16 / SPW;
+  const int s = lane / kLanesPerSlot;
+  const int e = __shfl_sync(0xFFFFFFFFu, e_lane, s & (SPW - 1));
+  if (lane < 16 && lane % kLanesPerSlot == 0 && s < nslots) {
+    const size_t out = ((size_t)t * top_k + j0 + s) * I + n;
+    if (e >= 0 && e < E) {
+      const float g = tot * unscale, uu = up_tot * unscale;
+      const float sl = g / (1.0f + expf(-g));
+      const __nv_bfloat16 hv = __float2bfloat16_rn(sl * uu);
+      h[out] = *reinterpret_cast<const uint16_t*>(&hv);
+    } else {
+      h[out] = 0;
+      flag_invalid(err);
+    }
   }
 }
 
@@ -416,15 +439,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     ba = bc;
     u0 += 64;
   }
-#pragma unroll
-  for (int r = 0; r < OPW; ++r) acc[r] = warp_sum(acc[r]) * unscale;
+  // lane l holds the total of output l / (32 / OPW)
+  const float tot = warp_sum_transposed<OPW>(acc) * unscale;
   if (bad) flag_invalid(err);
-  if (lane < OPW) {
-    float v = acc[0];
-#pragma unroll
-    for (int r = 1; r < OPW; ++r) v = (lane == r) ? acc[r] : v;
-    y[(size_t)t * H + o0 + lane] = v;
-  }
+  if (lane % (32 / OPW) == 0) y[(size_t)t * H + o0 + lane / (32 / OPW)] = tot;
 }
 
 // ------------------------------------------------------------- host side ---
@@ -444,6 +462,10 @@ moe_status check_shape(const moe_shape* s, int32_t B) {
   if (s->H <= 0 || s->I <= 0 || s->E <= 0 || s->top_k <= 0 || s->top_k > s->E || B < 0 ||
       s->H % 32 || s->I % 32) {
     set_error_msg("shape: need H%32==0, I%32==0, E>=1, 1<=top_k<=E, B>=0");
+    return MOE_ERR_SHAPE;
+  }
+  if (s->H > 8192) {
+    set_error_msg("shape: H above 8192 is not supported");
     return MOE_ERR_SHAPE;
   }
   // grid limits: pairs on grid.x (<= 2^31-1), neuron/output blocks on grid.y (<= 65535)
@@ -507,18 +529,30 @@ int pick_opw(int B, int H) {
   return 1;
 }
 
-template <int SPW>
+template <int SPW, int NSEG>
 moe_status launch_gate_up(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                           const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
                           cudaStream_t st) {
   const size_t smem = (size_t)s->H * 2;
-  moe_status rc = allow_smem(moe_gate_up_kernel<SPW>, smem);
+  moe_status rc = allow_smem(moe_gate_up_kernel<SPW, NSEG>, smem);
   if (rc != MOE_OK) return rc;
   const int groups = (s->top_k + SPW - 1) / SPW;
   const dim3 grid((unsigned)(B * groups), (unsigned)(s->I / kWarpsPerCta));
-  moe_gate_up_kernel<SPW><<<grid, kThreads, smem, st>>>(w->gu_codes, w->gu_scales, x, ids, h,
-                                                        err, s->H, s->I, s->E, s->top_k);
+  moe_gate_up_kernel<SPW, NSEG><<<grid, kThreads, smem, st>>>(
+      w->gu_codes, w->gu_scales, x, ids, h, err, s->H, s->I, s->E, s->top_k);
   return MOE_OK;
+}
+
+template <int NSEG>
+moe_status launch_gate_up_spw(const moe_shape* s, const moe_weights* w, const uint16_t* x,
+                              const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
+                              cudaStream_t st) {
+  switch (pick_spw(B, s->top_k, s->I)) {
+    case 8: return launch_gate_up<8, NSEG>(s, w, x, ids, B, h, err, st);
+    case 4: return launch_gate_up<4, NSEG>(s, w, x, ids, B, h, err, st);
+    case 2: return launch_gate_up<2, NSEG>(s, w, x, ids, B, h, err, st);
+    default: return launch_gate_up<1, NSEG>(s, w, x, ids, B, h, err, st);
+  }
 }
 
 template <int OPW>
@@ -556,12 +590,10 @@ moe_status gate_up_impl(const moe_shape* s, const moe_weights* w, const uint16_t
     set_error_msg("alignment: x and h need 16 bytes, ids and err_flag 4");
     return MOE_ERR_ALIGN;
   }
-  switch (pick_spw(B, s->top_k, s->I)) {
-    case 8: rc = launch_gate_up<8>(s, w, x, ids, B, h, err, st); break;
-    case 4: rc = launch_gate_up<4>(s, w, x, ids, B, h, err, st); break;
-    case 2: rc = launch_gate_up<2>(s, w, x, ids, B, h, err, st); break;
-    default: rc = launch_gate_up<1>(s, w, x, ids, B, h, err, st); break;
-  }
+  const int nseg = ((s->H >> 5) + kSegBlocks - 1) / kSegBlocks;  // 2048-element row segments
+  if (nseg == 1) rc = launch_gate_up_spw<1>(s, w, x, ids, B, h, err, st);
+  else if (nseg == 2) rc = launch_gate_up_spw<2>(s, w, x, ids, B, h, err, st);
+  else rc = launch_gate_up_spw<4>(s, w, x, ids, B, h, err, st);
   if (rc != MOE_OK) return rc;
   return launch_status("moe_gate_up launch");
 }

@@ -47,7 +47,8 @@ def test_host_validation_rejects_before_launch():
     assert gate_up(None, w, P, P, 1, P) == 1  # MOE_ERR_NULL
     assert gate_up(sh, None, P, P, 1, P) == 1
     assert gate_up(sh, w, None, P, 1, P) == 1
-    for bad in ((250, 128, 8, 2), (256, 100, 8, 2), (256, 128, 0, 1), (256, 128, 8, 9), (256, 128, 8, 0)):
+    for bad in ((250, 128, 8, 2), (256, 100, 8, 2), (256, 128, 0, 1), (256, 128, 8, 9), (256, 128, 8, 0),
+                (8224, 128, 8, 2)):
         assert gate_up(ops.make_shape(*bad), w, P, P, 1, P) == 2  # MOE_ERR_SHAPE
     assert gate_up(sh, w, P, P, -1, P) == 2
     assert gate_up(sh, _fake_weights(aligned=False), P, P, 1, P) == 3  # MOE_ERR_ALIGN
