@@ -29,9 +29,11 @@
 //    1 KB of one row contiguously. Weight loads bypass L1 allocation; reuse of
 //    a row by several tokens happens in L2, which the grid order makes likely
 //    (neuron/output block is the slow grid axis, tokens the fast one).
-//  * Latency. moe_gate_up warps loop over several routed slots of one token and
-//    prefetch the next unit's rows into registers while computing the current
-//    one, so each warp keeps HBM requests in flight; moe_down warps own several
+//  * Latency is hidden by occupancy: both kernels are kept at <= 80 registers
+//    so that 3 CTAs (24 warps) fit on an SM. (Holding a second unit of codes in
+//    registers to prefetch it, or staging codes through a cp.async ring in
+//    shared memory, both measured slower on this part.) moe_gate_up warps loop
+//    over several routed slots of one token; moe_down warps own several
 //    outputs that share one read of the intermediate from shared memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -240,10 +242,10 @@ __device__ __forceinline__ float warp_sum_transposed(float (&v)[V]) {
 // routed slots of its group. Dynamic shared memory: H f16 (the scaled x row).
 //
 // A warp's work is SPW * NSEG units (slot, segment of 2048 row elements),
-// unrolled at compile time; the gate and up codes of unit u+1 are loaded into
-// registers while unit u is computed. Each lane keeps one (gate, up) partial
-// pair per slot; all of them are reduced together at the end and the SwiGLU
-// epilogue of the SPW neurons runs once, in SPW lanes side by side.
+// unrolled at compile time: load the unit's gate and up codes, then consume
+// them. Each lane keeps one (gate, up) partial pair per slot; all of them are
+// reduced together at the end and the SwiGLU epilogue of the SPW neurons runs
+// once, in SPW lanes side by side.
 
 struct GateUpUnit {
   Codes32 g[kSegBlocksPerLane], u[kSegBlocksPerLane];
@@ -251,7 +253,7 @@ struct GateUpUnit {
 };
 
 template <int SPW, int NSEG>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     moe_gate_up_kernel(const uint8_t* __restrict__ gu_codes,
                        const uint8_t* __restrict__ gu_scales,
                        const uint16_t* __restrict__ x, const int32_t* __restrict__ ids,
@@ -311,12 +313,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   };
 
   constexpr int kUnits = SPW * NSEG;
-  GateUpUnit buf[2];
-  load_unit(0, 0, buf[0]);
 #pragma unroll
   for (int u = 0; u < kUnits; ++u) {
-    if (u + 1 < kUnits) load_unit((u + 1) / NSEG, (u + 1) % NSEG, buf[(u + 1) & 1]);
-    compute_unit(u / NSEG, u % NSEG, buf[u & 1]);
+    GateUpUnit U;
+    load_unit(u / NSEG, u % NSEG, U);
+    compute_unit(u / NSEG, u % NSEG, U);
   }
 
   // lane l now holds the total of value l >> (4 - log2 SPW): gate sums in
@@ -359,7 +360,7 @@ struct DownUnit {
 };
 
 template <int OPW>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     moe_down_kernel(const uint8_t* __restrict__ d_codes, const uint8_t* __restrict__ d_scales,
                     const uint16_t* __restrict__ h, const int32_t* __restrict__ ids,
                     const float* __restrict__ wts, float* __restrict__ y,
@@ -419,25 +420,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   };
 
-  DownUnit<OPW> A, B;
   int ja = lane / nblk, ba = lane - (lane / nblk) * nblk;  // this lane's first unit
-  int u0 = lane;
-  if (u0 < units) load_unit(ja, ba, A);
-  while (u0 < units) {
-    int jb = ja, bbv = ba;
-    advance(jb, bbv);
-    const bool has_b = u0 + 32 < units;
-    if (has_b) load_unit(jb, bbv, B);
-    compute_unit(ja, ba, A);
-    if (!has_b) break;
-    int jc = jb, bc = bbv;
-    advance(jc, bc);
-    const bool has_c = u0 + 64 < units;
-    if (has_c) load_unit(jc, bc, A);
-    compute_unit(jb, bbv, B);
-    ja = jc;
-    ba = bc;
-    u0 += 64;
+  for (int u0 = lane; u0 < units; u0 += 32) {
+    DownUnit<OPW> U;
+    load_unit(ja, ba, U);
+    compute_unit(ja, ba, U);
+    advance(ja, ba);
   }
   // lane l holds the total of output l / (32 / OPW)
   const float tot = warp_sum_transposed<OPW>(acc) * unscale;
