@@ -42,8 +42,8 @@ METRIC = "MoE-layer decode tokens/s and achieved HBM GB/s (% of GB300 peak) at B
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="q30_b32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -108,10 +108,40 @@ def ncu_traffic(kernel: str, workload: str):
     return ent.get("dram_bytes_per_launch")
 
 
+# ------------------------------------------------------------ multi-rank --
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    """The slowest rank's time: every rank's value, reduced with MAX."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank_per_step: int, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: the tokens all ranks processed over the slowest
+    rank's time (replicas: every rank runs its own batches, weak scaling)."""
+    return tokens_per_rank_per_step * world * steps / (max_ms / 1e3)
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each replica draws its own token batches."""
+    return seed + 1000 * rank
+
+
 # ----------------------------------------------------------------- clocks --
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle-reason samples every 20 ms, timestamped; started
+    before the warm-up (nvidia-smi takes a moment to start) and stopped after
+    the timed region. Samples whose timestamp falls inside the timed region
+    (host wall clock from the first launch to the closing synchronize) are the
+    ones "under load"."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -123,10 +153,11 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except FileNotFoundError:
             self.proc = None
+        time.sleep(1.0)
         return self
 
     def __exit__(self, *a):
@@ -140,25 +171,43 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [l for l in out.splitlines() if l.strip()]
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
+    @staticmethod
+    def _epoch(ts: str):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(ts.strip(), fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def summary(self, t0: float, t1: float):
+        sm, mx, reasons, power = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in self.lines:
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                clk, mxv = float(f[1]), float(f[2])
             except ValueError:
                 continue
+            mx = mxv
+            when = self._epoch(f[0])
+            if when is None or not (t0 <= when <= t1):  # outside the timed region
+                continue
+            sm.append(clk)
+            try:
+                power.append(float(f[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
 # ---------------------------------------------------------- workload setup --
@@ -280,7 +329,7 @@ def run_ours(args, wl, rank, world, local_rank):
     s = wl.shape
     seed = 0
     layers = build_device_layers(s, N_LAYERS, seed, dev)
-    batches = make_batches(wl, N_BATCHES, seed + 1000 * rank)
+    batches = make_batches(wl, N_BATCHES, rank_seed(seed, rank))
     dx = [torch.from_numpy(b[0].view(np.int16)).to(dev) for b in batches]
     dids = [torch.from_numpy(b[1]).to(dev) for b in batches]
     dw = [torch.from_numpy(b[2]).to(dev) for b in batches]
@@ -298,33 +347,27 @@ def run_ours(args, wl, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def max_over_ranks(v: float) -> float:
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    for i in range(max(3, args.warmup)):
-        step(i)
-    barrier()
-
-    # ---- main timed region: K whole-layer steps --------------------------
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         gpu_id = str(local_rank)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(gpu_id) as clk:
+        for i in range(max(3, args.warmup)):
+            step(i)
         barrier()
+        # ---- main timed region: K whole-layer steps ----------------------
+        barrier()
+        wall0 = time.time()
         ev0.record(stream)
         for i in range(args.steps):
             step(i)
         ev1.record(stream)
         barrier()
-    el_ms = max_over_ranks(ev0.elapsed_time(ev1))
+        wall1 = time.time()
+    el_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     ms_per_step = el_ms / args.steps
-    value = wl.B * world * args.steps / (el_ms / 1e3)
+    value = job_tokens_per_s(wl.B, world, args.steps, el_ms)
     if int(err.item()) != 0:
         raise RuntimeError("device error flag set: an expert id was out of range")
 
@@ -373,8 +416,8 @@ def run_ours(args, wl, rank, world, local_rank):
         e2e_step(i)
     e1.record(stream)
     barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
-    e2e_value = wl.B * world * args.steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = job_tokens_per_s(wl.B, world, args.steps, e2e_ms)
     h2d = px[0].numel() * 2 + pids[0].numel() * 4 + pw[0].numel() * 4
     d2h = py.numel() * 4
 
@@ -410,7 +453,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clk.summary(wall0, wall1),
     }
     print(json.dumps(out), flush=True)
 

@@ -204,6 +204,19 @@ __device__ int stage_activations(const uint16_t* __restrict__ src, int rows, int
   return sigma;
 }
 
+// Programmatic dependent launch (moe_layer launches moe_down as a dependent of
+// moe_gate_up). launch_dependents lets the dependent grid be scheduled once
+// every CTA of this grid has issued it; wait_prerequisite blocks until the
+// prerequisite grid has completed and its writes are visible (it returns at
+// once when the kernel was not launched as a dependent). Both are hardware
+// grid dependencies, not spins on memory.
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_prerequisite() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_invalid(int32_t* err) {
   if (err) atomicOr(err, 1);
 }
@@ -269,11 +282,10 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int nblk = H >> 5;
   const int nslots = min(SPW, top_k - j0);
 
+  launch_dependents();
+
   // lane s < nslots holds the expert id of slot s; -1 marks "no slot"
   const int e_lane = (lane < nslots) ? __ldg(ids + (size_t)t * top_k + j0 + lane) : -1;
-
-  const int sigma = stage_activations(x + (size_t)t * H, 1, H, xs, red);
-  const float unscale = exp2i(-sigma);
 
   auto load_unit = [&](int s, int seg, GateUpUnit& U) {
     const int e = __shfl_sync(0xFFFFFFFFu, e_lane, s);
@@ -313,11 +325,15 @@ __global__ void __launch_bounds__(kThreads, 3)
   };
 
   constexpr int kUnits = SPW * NSEG;
+  // the first unit's codes are requested before the activation prologue
+  GateUpUnit U;
+  load_unit(0, 0, U);
+  const int sigma = stage_activations(x + (size_t)t * H, 1, H, xs, red);
+  const float unscale = exp2i(-sigma);
 #pragma unroll
   for (int u = 0; u < kUnits; ++u) {
-    GateUpUnit U;
-    load_unit(u / NSEG, u % NSEG, U);
     compute_unit(u / NSEG, u % NSEG, U);
+    if (u + 1 < kUnits) load_unit((u + 1) / NSEG, (u + 1) % NSEG, U);
   }
 
   // lane l now holds the total of value l >> (4 - log2 SPW): gate sums in
@@ -360,7 +376,7 @@ struct DownUnit {
 };
 
 template <int OPW>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, OPW >= 8 ? 2 : 3)
     moe_down_kernel(const uint8_t* __restrict__ d_codes, const uint8_t* __restrict__ d_scales,
                     const uint16_t* __restrict__ h, const int32_t* __restrict__ ids,
                     const float* __restrict__ wts, float* __restrict__ y,
@@ -375,21 +391,13 @@ __global__ void __launch_bounds__(kThreads, 3)
   int* s_ids = reinterpret_cast<int*>(dyn + (size_t)top_k * (I >> 3));  // top_k
   float* s_w = reinterpret_cast<float*>(s_ids + top_k);                 // top_k
 
-  for (int j = threadIdx.x; j < top_k; j += kThreads) {
-    s_ids[j] = __ldg(ids + (size_t)t * top_k + j);
-    s_w[j] = __ldg(wts + (size_t)t * top_k + j);
-  }
-  const int sigma = stage_activations(h + (size_t)t * top_k * I, top_k, I, hs, red);
-  const float unscale = exp2i(-sigma);
-
   const int units = top_k * nblk;
   float acc[OPW];
 #pragma unroll
   for (int r = 0; r < OPW; ++r) acc[r] = 0.0f;
   bool bad = false;
 
-  auto load_unit = [&](int jj, int bb, DownUnit<OPW>& U) {
-    const int e = s_ids[jj];
+  auto load_unit = [&](int e, int bb, DownUnit<OPW>& U) {
     if (e < 0 || e >= E) return;
 #pragma unroll
     for (int r = 0; r < OPW; ++r) {
@@ -420,12 +428,24 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
   };
 
+  // The ids, routing weights and down weights are inputs of the layer, not
+  // produced by moe_gate_up: this lane's first unit is requested before
+  // waiting for the intermediate.
   int ja = lane / nblk, ba = lane - (lane / nblk) * nblk;  // this lane's first unit
+  DownUnit<OPW> U;
+  if (lane < units) load_unit(__ldg(ids + (size_t)t * top_k + ja), ba, U);
+  for (int j = threadIdx.x; j < top_k; j += kThreads) {
+    s_ids[j] = __ldg(ids + (size_t)t * top_k + j);
+    s_w[j] = __ldg(wts + (size_t)t * top_k + j);
+  }
+  wait_prerequisite();  // the intermediate h is complete from here on
+  const int sigma = stage_activations(h + (size_t)t * top_k * I, top_k, I, hs, red);
+  const float unscale = exp2i(-sigma);
+
   for (int u0 = lane; u0 < units; u0 += 32) {
-    DownUnit<OPW> U;
-    load_unit(ja, ba, U);
     compute_unit(ja, ba, U);
     advance(ja, ba);
+    if (u0 + 32 < units) load_unit(s_ids[ja], ba, U);
   }
   // lane l holds the total of output l / (32 / OPW)
   const float tot = warp_sum_transposed<OPW>(acc) * unscale;
@@ -507,8 +527,11 @@ int pick_spw(int B, int top_k, int I) {
   return 1;
 }
 
-// Outputs per warp of moe_down: as many as keep at least kMinCtas CTAs.
-int pick_opw(int B, int H) {
+// Outputs per warp of moe_down: 8 for rows of at most 1024 elements when at
+// least 6 CTAs per SM remain (measured faster there), else as many as keep
+// at least kMinCtas CTAs.
+int pick_opw(int B, int H, int I) {
+  if (I <= 1024 && (int64_t)B * (H / (kWarpsPerCta * 8)) >= 6 * 152) return 8;
   const int opws[3] = {4, 2, 1};
   for (int v : opws) {
     const int64_t ctas = (int64_t)B * (H / (kWarpsPerCta * v));
@@ -543,16 +566,32 @@ moe_status launch_gate_up_spw(const moe_shape* s, const moe_weights* w, const ui
   }
 }
 
+// dependent = true launches moe_down as a programmatic dependent of the kernel
+// before it on the stream (used by moe_layer, where that kernel is moe_gate_up
+// and only h is produced by it).
 template <int OPW>
 moe_status launch_down(const moe_shape* s, const moe_weights* w, const uint16_t* h,
                        const int32_t* ids, const float* wts, int32_t B, float* y, int32_t* err,
-                       cudaStream_t st) {
+                       cudaStream_t st, bool dependent) {
   const size_t smem = (size_t)s->top_k * s->I * 2 + (size_t)s->top_k * 8;
   moe_status rc = allow_smem(moe_down_kernel<OPW>, smem);
   if (rc != MOE_OK) return rc;
-  const dim3 grid((unsigned)B, (unsigned)(s->H / (kWarpsPerCta * OPW)));
-  moe_down_kernel<OPW><<<grid, kThreads, smem, st>>>(w->d_codes, w->d_scales, h, ids, wts, y,
-                                                     err, s->H, s->I, s->E, s->top_k);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)B, (unsigned)(s->H / (kWarpsPerCta * OPW)));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_down_kernel<OPW>, w->d_codes, w->d_scales, h,
+                                           ids, wts, y, err, s->H, s->I, s->E, s->top_k);
+  if (e != cudaSuccess) {
+    set_error("moe_down launch", e);
+    return MOE_ERR_CUDA;
+  }
   return MOE_OK;
 }
 
@@ -588,7 +627,7 @@ moe_status gate_up_impl(const moe_shape* s, const moe_weights* w, const uint16_t
 
 moe_status down_impl(const moe_shape* s, const moe_weights* w, const uint16_t* h,
                      const int32_t* ids, const float* wts, int32_t B, float* y, int32_t* err,
-                     cudaStream_t st) {
+                     cudaStream_t st, bool dependent) {
   moe_status rc = check_shape(s, B);
   if (rc != MOE_OK) return rc;
   if ((rc = check_weights(w, false, true)) != MOE_OK) return rc;
@@ -599,10 +638,11 @@ moe_status down_impl(const moe_shape* s, const moe_weights* w, const uint16_t* h
     set_error_msg("alignment: h needs 16 bytes, ids/wts/y/err_flag 4");
     return MOE_ERR_ALIGN;
   }
-  switch (pick_opw(B, s->H)) {
-    case 4: rc = launch_down<4>(s, w, h, ids, wts, B, y, err, st); break;
-    case 2: rc = launch_down<2>(s, w, h, ids, wts, B, y, err, st); break;
-    default: rc = launch_down<1>(s, w, h, ids, wts, B, y, err, st); break;
+  switch (pick_opw(B, s->H, s->I)) {
+    case 8: rc = launch_down<8>(s, w, h, ids, wts, B, y, err, st, dependent); break;
+    case 4: rc = launch_down<4>(s, w, h, ids, wts, B, y, err, st, dependent); break;
+    case 2: rc = launch_down<2>(s, w, h, ids, wts, B, y, err, st, dependent); break;
+    default: rc = launch_down<1>(s, w, h, ids, wts, B, y, err, st, dependent); break;
   }
   if (rc != MOE_OK) return rc;
   return launch_status("moe_down launch");
@@ -619,7 +659,7 @@ extern "C" moe_status moe_gate_up(const moe_shape* shape, const moe_weights* w,
 extern "C" moe_status moe_down(const moe_shape* shape, const moe_weights* w, const uint16_t* h,
                                const int32_t* ids, const float* wts, int32_t B, float* y,
                                int32_t* err_flag, void* stream) {
-  return down_impl(shape, w, h, ids, wts, B, y, err_flag, (cudaStream_t)stream);
+  return down_impl(shape, w, h, ids, wts, B, y, err_flag, (cudaStream_t)stream, false);
 }
 
 extern "C" moe_status moe_layer(const moe_shape* shape, const moe_weights* w, const uint16_t* x,
@@ -634,7 +674,7 @@ extern "C" moe_status moe_layer(const moe_shape* shape, const moe_weights* w, co
   if (!x || !ids || !wts || !h_scratch || !y) return MOE_ERR_NULL;
   rc = gate_up_impl(shape, w, x, ids, B, h_scratch, err_flag, (cudaStream_t)stream);
   if (rc != MOE_OK) return rc;
-  return down_impl(shape, w, h_scratch, ids, wts, B, y, err_flag, (cudaStream_t)stream);
+  return down_impl(shape, w, h_scratch, ids, wts, B, y, err_flag, (cudaStream_t)stream, true);
 }
 
 extern "C" moe_status moe_layer_host(const moe_shape* shape, const moe_weights* w,
@@ -755,5 +795,5 @@ extern "C" moe_status moe_layer_noalloc(const moe_shape* shape, const moe_weight
   // id) before moe_down reads it on the same stream: nothing needs clearing
   rc = gate_up_impl(shape, w, x, ids, B, h, err_flag, (cudaStream_t)stream);
   if (rc != MOE_OK) return rc;
-  return down_impl(shape, w, h, ids, wts, B, y, err_flag, (cudaStream_t)stream);
+  return down_impl(shape, w, h, ids, wts, B, y, err_flag, (cudaStream_t)stream, true);
 }
