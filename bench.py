@@ -49,6 +49,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work the oracle baseline sample aims at")
+    ap.add_argument("--sweep", nargs="*", default=None,
+                    help="instead of the single contract line, print one line per workload "
+                         "(default: the batch sweep of the pages' metric), timing CUDA-graph "
+                         "replays of the layer")
     return ap.parse_args()
 
 
@@ -458,8 +462,78 @@ def run_ours(args, wl, rank, world, local_rank):
     print(json.dumps(out), flush=True)
 
 
+SWEEP_DEFAULT = ([f"q30_{r}_b{b}" for r in ("uniform", "skewed") for b in (1, 2, 4, 8, 16, 32, 64)]
+                 + ["q235_b1", "q235_b16", "q235_b64", "tiny_b1"])
+
+
+def run_sweep(names, steps: int):
+    """Per workload: the layer (moe_layer, both kernels) captured in a CUDA graph
+    over a rotation of 2 layers x 8 token batches, replayed; CUDA-event time per
+    step. Launch overhead of the host is outside the measurement, as in a
+    graph-driven decode loop."""
+    import torch
+
+    from output_centric_expert_gb300 import ops, workload
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, _ = measured_peaks()
+    built = {}
+    for name in names:
+        wl = workload.WORKLOADS[name]
+        s = wl.shape
+        key = (s.H, s.I, s.E, s.top_k)
+        if key not in built:
+            built.clear()
+            torch.cuda.empty_cache()
+            built[key] = build_device_layers(s, N_LAYERS, 0, dev)
+        layers = built[key]
+        batches = make_batches(wl, N_BATCHES, 0)
+        dx = [torch.from_numpy(b[0].view(np.int16)).to(dev) for b in batches]
+        dids = [torch.from_numpy(b[1]).to(dev) for b in batches]
+        dw = [torch.from_numpy(b[2]).to(dev) for b in batches]
+        h = torch.empty((wl.B, s.top_k, s.I), dtype=torch.int16, device=dev)
+        y = torch.empty((wl.B, s.H), dtype=torch.float32, device=dev)
+        rot = 2 * N_BATCHES  # steps per graph replay
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for i in range(rot):  # warm-up outside capture
+                ops.moe_layer(layers[i % N_LAYERS], dx[i % N_BATCHES], dids[i % N_BATCHES],
+                              dw[i % N_BATCHES], h, y)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(rot):
+                ops.moe_layer(layers[i % N_LAYERS], dx[i % N_BATCHES], dids[i % N_BATCHES],
+                              dw[i % N_BATCHES], h, y)
+        reps = max(3, steps // rot)
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / (reps * rot)
+        lay_bytes = float(np.mean([layer_bytes(s, b[1]) for b in batches]))
+        uniq = float(np.mean([len(np.unique(b[1])) for b in batches]))
+        print(json.dumps({"workload": name, "H": s.H, "I": s.I, "E": s.E, "top_k": s.top_k,
+                          "B": wl.B, "routing": wl.routing, "us_per_layer": round(us, 2),
+                          "tokens_per_s": round(wl.B / us * 1e6), "unique_experts": uniq,
+                          "layer_bytes": lay_bytes, "layer_gbs": round(lay_bytes / us / 1e3, 1),
+                          "frac_of_measured_peak": round(lay_bytes / us / 1e3 / peak, 4),
+                          "timing": "CUDA graph of 16 steps (2 layers x 8 batches), replayed"}),
+              flush=True)
+
+
 def main():
     args = parse()
+    if args.sweep is not None:
+        run_sweep(args.sweep or SWEEP_DEFAULT, args.steps)
+        return
     from output_centric_expert_gb300 import workload
     wl = workload.WORKLOADS[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
