@@ -207,6 +207,34 @@ def test_invalid_ids_flagged_and_skipped(tiny):
     _check_h(h, h_ref)
 
 
+@pytest.mark.parametrize("which,B,routing", [("q30", 32, "uniform"), ("q30", 64, "skewed"), ("tiny", 16, "uniform")])
+def test_batch_equals_tokens_one_at_a_time(request, which, B, routing):
+    """A large batch runs with several slots per gate_up warp and several outputs
+    per down warp; a single token with one of each. Every (token, neuron) and
+    (token, output) sum is formed in the same order, so results must be identical."""
+    layer = request.getfixturevalue(which)
+    x, ids, w = workload.tokens(layer.shape, B, routing=routing, batch=500 + B)
+    y, h = _run_layer(layer, x, ids, w)
+    for t in range(B):
+        y1, h1 = _run_layer(layer, x[t:t + 1], ids[t:t + 1], w[t:t + 1])
+        assert np.array_equal(h1[0], h[t]), t
+        assert np.array_equal(y1[0], y[t]), t
+
+
+def test_invalid_ids_in_a_large_batch(tiny):
+    B = 24  # several slots per gate_up warp
+    x, ids, w = workload.tokens(tiny.shape, B, batch=7)
+    ids = ids.copy()
+    ids[3, 0] = 8
+    ids[17, 1] = -1
+    y, h, err = _run_layer(tiny, x, ids, w, with_err=True)
+    y_ref, h_ref, bad = oracle.moe_layer(tiny.ref, x, ids, w, return_h=True)
+    assert bad == 2 and err == 1
+    assert np.all(h[3, 0] == 0) and np.all(h[17, 1] == 0)
+    _check_y(y, y_ref)
+    _check_h(h, h_ref)
+
+
 def test_empty_batch_launches_nothing(tiny):
     y = torch.full((0, tiny.shape.H), 7.0, device="cuda")
     ops.moe_layer(tiny.dev, torch.empty((0, tiny.shape.H), dtype=torch.int16, device="cuda"),
