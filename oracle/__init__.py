@@ -64,6 +64,8 @@ def _get():
             lib.oracle_dequantize_mxfp8.argtypes = [vp, vp, i64, i64, vp]
             lib.oracle_moe_layer.restype = i64
             lib.oracle_moe_layer.argtypes = [i32, i32, i32, i32, i32] + [vp] * 11
+            lib.oracle_moe_layer_variant.restype = i64
+            lib.oracle_moe_layer_variant.argtypes = [i32, i32, i32, i32, i32] + [vp] * 9 + [i32, i32, vp]
             _lib = lib
         return _lib
 
@@ -164,3 +166,26 @@ def moe_layer(layer: QuantizedLayer, x_bits: np.ndarray, ids: np.ndarray, w: np.
     if n_bad < 0:
         raise ValueError("oracle_moe_layer rejected the shape (H and I must be multiples of 32)")
     return (y, h, int(n_bad)) if return_h else (y, int(n_bad))
+
+
+def moe_layer_variant(layer: QuantizedLayer, x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray,
+                      round_h: bool, mx_acts: bool) -> np.ndarray:
+    """The layer with the intermediate rounded to BF16 or kept exact, and with or
+    without an MXFP8 round trip of each projection's input activation (the
+    conventional path's BF16 -> MXFP8 -> BF16). round_h=True, mx_acts=False is
+    the layer itself. Returns y [B,H] float64."""
+    x_bits = _c(x_bits, np.uint16)
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float32)
+    B, H = x_bits.shape
+    k = ids.shape[1]
+    y = np.empty((B, H), dtype=np.float64)
+    n = _get().oracle_moe_layer_variant(
+        layer.H, layer.I, layer.E, k, B, x_bits.ctypes.data, ids.ctypes.data, w.ctypes.data,
+        layer.gate_codes.ctypes.data, layer.gate_scales.ctypes.data,
+        layer.up_codes.ctypes.data, layer.up_scales.ctypes.data,
+        layer.down_codes.ctypes.data, layer.down_scales.ctypes.data,
+        int(round_h), int(mx_acts), y.ctypes.data)
+    if n < 0:
+        raise ValueError("oracle_moe_layer_variant rejected the shape")
+    return y

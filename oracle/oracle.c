@@ -292,3 +292,98 @@ int64_t oracle_moe_layer(int32_t H, int32_t I, int32_t E, int32_t k, int32_t B,
   free(hbits);
   return invalid;
 }
+
+/* ---------- Variants for the accuracy study --------------------------------
+ * "Better MoE model inference with warp decode", Key claims [§Improved
+ * accuracy] (and the sd114.wiki page, 性能与精度双重提升, item 2): the
+ * conventional path quantises each BF16 activation to MXFP8 before a
+ * projection and back (a BF16 -> MXFP8 -> BF16 round trip); warp decode keeps
+ * activations in BF16 with FP32 accumulators, and its output is reported
+ * closer to a full-precision reference.
+ *
+ * The same layer as oracle_moe_layer, with two switches:
+ *   round_h : 1 = the intermediate is rounded to BF16 (the layer's own rule),
+ *             0 = it is kept exact (a full-precision reference);
+ *   mx_acts : 1 = the activation entering each projection (x for gate/up, the
+ *             intermediate for down) is first replaced by its MXFP8 round
+ *             trip (OCP MX v1.0 conversion, as in oracle_quantize_mxfp8);
+ *             0 = it is used as is.
+ * oracle_moe_layer equals round_h = 1, mx_acts = 0. y [B][H] is written;
+ * returns the number of out-of-range slots, or -1 on a bad shape.
+ */
+static void mx_roundtrip(double* v, int64_t K) {
+  for (int64_t b = 0; b < K / 32; ++b) {
+    double* blk = v + b * 32;
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i)
+      if (fabs(blk[i]) > amax) amax = fabs(blk[i]);
+    int s;
+    if (amax == 0.0) {
+      s = 0;
+    } else if (isinf(amax)) {
+      s = 254;
+    } else {
+      int ex;
+      frexp(amax, &ex);
+      s = (ex - 1) - 8 + 127;
+      if (s < 0) s = 0;
+      if (s > 254) s = 254;
+    }
+    double X = ldexp(1.0, s - 127);
+    for (int i = 0; i < 32; ++i) blk[i] = e4m3_table[e4m3_nearest(blk[i] / X)] * X;
+  }
+}
+
+int64_t oracle_moe_layer_variant(int32_t H, int32_t I, int32_t E, int32_t k, int32_t B,
+                                 const uint16_t* x, const int32_t* ids, const float* wts,
+                                 const uint8_t* gate_codes, const uint8_t* gate_scales,
+                                 const uint8_t* up_codes, const uint8_t* up_scales,
+                                 const uint8_t* down_codes, const uint8_t* down_scales,
+                                 int32_t round_h, int32_t mx_acts, double* y) {
+  if (H <= 0 || I <= 0 || E <= 0 || k <= 0 || B < 0 || H % 32 || I % 32) return -1;
+  fill_tables();
+  int64_t invalid = 0;
+  const int64_t hb = H / 32, ib = I / 32;
+  double* xval = (double*)malloc(sizeof(double) * (size_t)H);
+  double* hval = (double*)malloc(sizeof(double) * (size_t)I);
+  if (!xval || !hval) {
+    free(xval);
+    free(hval);
+    return -1;
+  }
+  for (int32_t t = 0; t < B; ++t) {
+    for (int32_t hh = 0; hh < H; ++hh) xval[hh] = oracle_bf16_value(x[(int64_t)t * H + hh]);
+    if (mx_acts) mx_roundtrip(xval, H);
+    double* yt = y + (int64_t)t * H;
+    for (int32_t o = 0; o < H; ++o) yt[o] = 0.0;
+    for (int32_t j = 0; j < k; ++j) {
+      int32_t e = ids[(int64_t)t * k + j];
+      if (e < 0 || e >= E) {
+        ++invalid;
+        continue;
+      }
+      for (int32_t n = 0; n < I; ++n) {
+        int64_t row = (int64_t)e * I + n;
+        double g = 0.0, u = 0.0;
+        for (int32_t hh = 0; hh < H; ++hh) {
+          g += xval[hh] * mx_element(gate_codes[row * H + hh], gate_scales[row * hb + hh / 32]);
+          u += xval[hh] * mx_element(up_codes[row * H + hh], up_scales[row * hb + hh / 32]);
+        }
+        double hv = oracle_silu(g) * u;
+        hval[n] = round_h ? oracle_bf16_value(oracle_bf16_rne(hv)) : hv;
+      }
+      if (mx_acts) mx_roundtrip(hval, I);
+      double wj = (double)wts[(int64_t)t * k + j];
+      for (int32_t o = 0; o < H; ++o) {
+        int64_t row = (int64_t)e * H + o;
+        double acc = 0.0;
+        for (int32_t i = 0; i < I; ++i)
+          acc += hval[i] * mx_element(down_codes[row * I + i], down_scales[row * ib + i / 32]);
+        yt[o] += wj * acc;
+      }
+    }
+  }
+  free(xval);
+  free(hval);
+  return invalid;
+}
