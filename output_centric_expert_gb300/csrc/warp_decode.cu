@@ -265,7 +265,9 @@ struct GateUpUnit {
   uint32_t sg[kSegBlocksPerLane], su[kSegBlocksPerLane];
 };
 
-template <int SPW, int NSEG>
+// FULL: every segment is whole (H a multiple of 2048), so no block index
+// needs checking against the row length.
+template <int SPW, int NSEG, bool FULL>
 __global__ void __launch_bounds__(kThreads, 3)
     moe_gate_up_kernel(const uint8_t* __restrict__ gu_codes,
                        const uint8_t* __restrict__ gu_scales,
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
     for (int q = 0; q < kSegBlocksPerLane; ++q) {
       const int b = seg * kSegBlocks + q * 32 + lane;
-      if (b < nblk) {
+      if (FULL || b < nblk) {
         U.g[q] = ld_codes32(gc + (size_t)b * 32);
         U.u[q] = ld_codes32(gc + H + (size_t)b * 32);
         U.sg[q] = __ldg(sc + b);
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
     for (int q = 0; q < kSegBlocksPerLane; ++q) {
       const int b = seg * kSegBlocks + q * 32 + lane;
-      if (b < nblk) {
+      if (FULL || b < nblk) {
         uint32_t a[16];
         ld_act_block(xs, nblk, b, a);
         acc[s] = fmaf(block_dot(a, U.g[q]), e8m0_to_f32(U.sg[q]), acc[s]);
@@ -540,18 +542,27 @@ int pick_opw(int B, int H, int I) {
   return 1;
 }
 
-template <int SPW, int NSEG>
+template <int SPW, int NSEG, bool FULL>
 moe_status launch_gate_up(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                           const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
                           cudaStream_t st) {
   const size_t smem = (size_t)s->H * 2;
-  moe_status rc = allow_smem(moe_gate_up_kernel<SPW, NSEG>, smem);
+  moe_status rc = allow_smem(moe_gate_up_kernel<SPW, NSEG, FULL>, smem);
   if (rc != MOE_OK) return rc;
   const int groups = (s->top_k + SPW - 1) / SPW;
   const dim3 grid((unsigned)(B * groups), (unsigned)(s->I / kWarpsPerCta));
-  moe_gate_up_kernel<SPW, NSEG><<<grid, kThreads, smem, st>>>(
+  moe_gate_up_kernel<SPW, NSEG, FULL><<<grid, kThreads, smem, st>>>(
       w->gu_codes, w->gu_scales, x, ids, h, err, s->H, s->I, s->E, s->top_k);
   return MOE_OK;
+}
+
+template <int SPW, int NSEG>
+moe_status launch_gate_up_full(const moe_shape* s, const moe_weights* w, const uint16_t* x,
+                               const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
+                               cudaStream_t st) {
+  if ((s->H >> 5) % kSegBlocks == 0)
+    return launch_gate_up<SPW, NSEG, true>(s, w, x, ids, B, h, err, st);
+  return launch_gate_up<SPW, NSEG, false>(s, w, x, ids, B, h, err, st);
 }
 
 template <int NSEG>
@@ -559,10 +570,10 @@ moe_status launch_gate_up_spw(const moe_shape* s, const moe_weights* w, const ui
                               const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
                               cudaStream_t st) {
   switch (pick_spw(B, s->top_k, s->I)) {
-    case 8: return launch_gate_up<8, NSEG>(s, w, x, ids, B, h, err, st);
-    case 4: return launch_gate_up<4, NSEG>(s, w, x, ids, B, h, err, st);
-    case 2: return launch_gate_up<2, NSEG>(s, w, x, ids, B, h, err, st);
-    default: return launch_gate_up<1, NSEG>(s, w, x, ids, B, h, err, st);
+    case 8: return launch_gate_up_full<8, NSEG>(s, w, x, ids, B, h, err, st);
+    case 4: return launch_gate_up_full<4, NSEG>(s, w, x, ids, B, h, err, st);
+    case 2: return launch_gate_up_full<2, NSEG>(s, w, x, ids, B, h, err, st);
+    default: return launch_gate_up_full<1, NSEG>(s, w, x, ids, B, h, err, st);
   }
 }
 
