@@ -464,6 +464,7 @@ def run_ours(args, wl, rank, world, local_rank):
 
 SWEEP_DEFAULT = ([f"q30_{r}_b{b}" for r in ("uniform", "skewed") for b in (1, 2, 4, 8, 16, 32, 64)]
                  + ["q235_b1", "q235_b16", "q235_b64", "tiny_b1"])
+SWEEP_VARIANTS = ["dsv3_b1", "dsv3_b16", "dsv3_b64", "mixtral_b1", "mixtral_b16", "mixtral_b64"]
 
 
 def run_sweep(names, steps: int):

@@ -56,6 +56,11 @@ SHAPES = {
     "tiny": LayerShape(256, 128, 8, 2),
     "q30": LayerShape(2048, 768, 128, 8),  # Qwen-3-30B-A3B-shaped layer
     "q235": LayerShape(4096, 1536, 128, 8),  # Qwen-3-235B-A22B-shaped layer
+    # shape variants ("Better MoE model inference with warp decode", Why it's
+    # interesting: does the flip carry over to fine-grained MoE such as
+    # DeepSeek-V3?): routed experts only, by shape
+    "dsv3": LayerShape(7168, 2048, 256, 8),  # DeepSeek-V3-shaped routed-expert layer
+    "mixtral": LayerShape(4096, 14336, 8, 2),  # Mixtral-8x7B-shaped layer (few, wide experts)
 }
 
 
@@ -84,6 +89,8 @@ WORKLOADS: dict[str, Workload] = {
     "q30_b32": Workload("q30_b32", SHAPES["q30"], 32),
     **_sweep(),
     **{f"q235_b{b}": Workload(f"q235_b{b}", SHAPES["q235"], b) for b in (1, 16, 64)},
+    **{f"dsv3_b{b}": Workload(f"dsv3_b{b}", SHAPES["dsv3"], b) for b in (1, 16, 64)},
+    **{f"mixtral_b{b}": Workload(f"mixtral_b{b}", SHAPES["mixtral"], b) for b in (1, 16, 64)},
 }
 
 

@@ -136,6 +136,23 @@ def test_q235_sampled_tokens():
     assert np.all(np.isfinite(y))
 
 
+@pytest.mark.parametrize("name,E,B", [("dsv3", 16, 12), ("mixtral", 8, 6)])
+def test_shape_variants(name, E, B):
+    """DeepSeek-V3-shaped (H=7168: partial row segments) and Mixtral-shaped
+    (I=14336: a 57 KB intermediate per token) layers, with fewer experts than the
+    models have (parity depends on the row shapes, not on E)."""
+    full = workload.SHAPES[name]
+    s = workload.LayerShape(full.H, full.I, E, full.top_k)
+    x, ids, w = workload.tokens(s, B, batch=11)
+    sample = [0, B // 2, B - 1]
+    layer = Layer(s, oracle_experts=np.unique(ids[sample]))
+    y, h = _run_layer(layer, x, ids, w)
+    y_ref, h_ref, _ = oracle.moe_layer(layer.ref, x[sample], ids[sample], w[sample], return_h=True)
+    _check_y(y[sample], y_ref)
+    _check_h(h[sample], h_ref)
+    assert np.all(np.isfinite(y))
+
+
 # ------------------------------------------------------------ edge cases ----
 
 def _rand_layer_shape(H, I, E, k, seed=0):
