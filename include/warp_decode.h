@@ -151,6 +151,34 @@ moe_status moe_layer_host(const moe_shape* shape, const moe_weights* w, const ui
                           float* y_dev, float* y_host, int32_t* err_flag, void* stream);
 
 /*
+ * moe_route -- the router in front of the layer: for every token, the top_k
+ * experts of softmax(logits) and their renormalised weights ("Better MoE
+ * model inference with warp decode", Method: each token is routed to the
+ * top-k of E experts, e.g. top-8 of 128).
+ *   logits [B][E]     FP32 router logits (device), finite
+ *   ids    [B][top_k] int32, written: experts by descending logit, ties to the
+ *                     lower index
+ *   wts    [B][top_k] FP32, written: exp(l_j - l_max) / sum over the chosen i
+ *                     of exp(l_i - l_max) (= the softmax renormalised over the
+ *                     chosen experts)
+ * Needs E <= 256 and top_k <= 32 (MOE_ERR_UNSUPPORTED otherwise).
+ */
+moe_status moe_route(const moe_shape* shape, const float* logits, int32_t B, int32_t* ids,
+                     float* wts, void* stream);
+
+/*
+ * moe_layer_routed -- the layer from router logits, still two kernels: every
+ * moe_gate_up and moe_down warp routes its token from `logits` itself (the
+ * same choice as moe_route), so no ids/weights array has to exist between
+ * router and layer. If ids_out and wts_out are both non-NULL, the routing is
+ * also written there ([B][top_k], as moe_route). Same limits as moe_route;
+ * other arguments as for moe_layer.
+ */
+moe_status moe_layer_routed(const moe_shape* shape, const moe_weights* w, const uint16_t* x,
+                            const float* logits, int32_t B, uint16_t* h_scratch, float* y,
+                            int32_t* ids_out, float* wts_out, int32_t* err_flag, void* stream);
+
+/*
  * moe_layer_noalloc -- the whole layer (as moe_layer) for callers that cannot
  * allocate device memory: code that runs inside a host framework which owns
  * every device allocation through its own pool, or a latency-critical decode

@@ -64,6 +64,8 @@ def _get():
             lib.oracle_dequantize_mxfp8.argtypes = [vp, vp, i64, i64, vp]
             lib.oracle_moe_layer.restype = i64
             lib.oracle_moe_layer.argtypes = [i32, i32, i32, i32, i32] + [vp] * 11
+            lib.oracle_route.restype = ctypes.c_int
+            lib.oracle_route.argtypes = [vp, i32, i32, i32, vp, vp]
             lib.oracle_moe_layer_variant.restype = i64
             lib.oracle_moe_layer_variant.argtypes = [i32, i32, i32, i32, i32] + [vp] * 9 + [i32, i32, vp]
             _lib = lib
@@ -189,3 +191,16 @@ def moe_layer_variant(layer: QuantizedLayer, x_bits: np.ndarray, ids: np.ndarray
     if n < 0:
         raise ValueError("oracle_moe_layer_variant rejected the shape")
     return y
+
+
+def route(logits: np.ndarray, top_k: int):
+    """Top-k routing of float32 logits [B,E]: ids int32 [B,k] (descending
+    probability, ties to the lower expert index) and renormalised softmax
+    weights float64 [B,k]."""
+    logits = _c(logits, np.float32)
+    B, E = logits.shape
+    ids = np.empty((B, top_k), dtype=np.int32)
+    w = np.empty((B, top_k), dtype=np.float64)
+    if _get().oracle_route(logits.ctypes.data, B, E, top_k, ids.ctypes.data, w.ctypes.data):
+        raise ValueError("oracle_route rejected its arguments")
+    return ids, w

@@ -387,3 +387,50 @@ int64_t oracle_moe_layer_variant(int32_t H, int32_t I, int32_t E, int32_t k, int
   free(hval);
   return invalid;
 }
+
+/* ---------- Router (the input of the layer) --------------------------------
+ * The tokens are routed to their top-k experts with renormalised softmax
+ * weights ("Better MoE model inference with warp decode", Method: tokens are
+ * routed to the top-k of E experts, e.g. top-8 of 128; sd114.wiki page,
+ * 传统路径的困境). Per token: p = softmax(logits) over the E experts; the k
+ * experts with the largest p, ties to the lower index, in descending order;
+ * w_j = p_j / sum of the chosen p. Double precision throughout.
+ */
+int oracle_route(const float* logits, int32_t B, int32_t E, int32_t k, int32_t* ids,
+                 double* w) {
+  if (B < 0 || E <= 0 || k <= 0 || k > E) return -1;
+  double* p = (double*)malloc(sizeof(double) * (size_t)E);
+  unsigned char* taken = (unsigned char*)calloc((size_t)E, 1);
+  if (!p || !taken) {
+    free(p);
+    free(taken);
+    return -1;
+  }
+  for (int32_t b = 0; b < B; ++b) {
+    const float* l = logits + (int64_t)b * E;
+    double mx = -INFINITY;
+    for (int32_t e = 0; e < E; ++e)
+      if ((double)l[e] > mx) mx = (double)l[e];
+    double z = 0.0;
+    for (int32_t e = 0; e < E; ++e) {
+      p[e] = exp((double)l[e] - mx);
+      z += p[e];
+    }
+    for (int32_t e = 0; e < E; ++e) p[e] /= z;
+    memset(taken, 0, (size_t)E);
+    double sum = 0.0;
+    for (int32_t j = 0; j < k; ++j) {
+      int32_t best = -1;
+      for (int32_t e = 0; e < E; ++e)
+        if (!taken[e] && (best < 0 || p[e] > p[best])) best = e;
+      taken[best] = 1;
+      ids[(int64_t)b * k + j] = best;
+      sum += p[best];
+    }
+    for (int32_t j = 0; j < k; ++j)
+      w[(int64_t)b * k + j] = p[ids[(int64_t)b * k + j]] / sum;
+  }
+  free(p);
+  free(taken);
+  return 0;
+}

@@ -221,6 +221,84 @@ __device__ __forceinline__ void flag_invalid(int32_t* err) {
   if (err) atomicOr(err, 1);
 }
 
+// ------------------------------------------------------------------ router --
+// Routing of one token from its router logits (the step in front of the layer:
+// "Better MoE model inference with warp decode", Method: each token goes to
+// the top-k of E experts). The renormalised top-k of softmax(logits) equals a
+// softmax over the k largest logits, so the experts are chosen on the logits
+// themselves (largest first, ties to the lower index) and
+//   w_j = exp(l_j - l_max) / sum over the chosen i of exp(l_i - l_max).
+// One warp; lane j < top_k receives the j-th choice. E <= 256, top_k <= 32,
+// logits finite.
+constexpr int kRouteMaxE = 256;
+
+struct RouteArgs {
+  const float* logits;  // [B][E], or nullptr: the ids/wts arrays are the routing
+  int32_t* ids_out;     // routing chosen by the kernel, written if non-null
+  float* w_out;
+};
+
+__device__ __noinline__ void warp_route(const float* __restrict__ row, int E, int top_k,
+                                           int& id, float& weight) {
+  constexpr int kPer = kRouteMaxE / 32;
+  const int lane = threadIdx.x & 31;
+  float v[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) v[i] = (lane + 32 * i < E) ? __ldg(row + lane + 32 * i) : 0.0f;
+  uint32_t open = 0;  // bit i: candidate lane + 32 i still available
+#pragma unroll
+  for (int i = 0; i < kPer; ++i)
+    if (lane + 32 * i < E) open |= 1u << i;
+  id = -1;
+  float mine = 0.0f, lmax = 0.0f;
+  for (int j = 0; j < top_k; ++j) {
+    float bv = 0.0f;
+    int be = 0x7FFFFFFF;  // none
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (((open >> i) & 1u) && (be == 0x7FFFFFFF || v[i] > bv)) {
+        bv = v[i];
+        be = lane + 32 * i;
+      }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, m);
+      const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, m);
+      if (oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be))) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) open &= ~(1u << (be >> 5));
+    if (lane == j) {
+      id = be;
+      mine = bv;
+    }
+    if (j == 0) lmax = bv;
+  }
+  float ex = (lane < top_k) ? expf(mine - lmax) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, m);
+  weight = ex / sum;
+}
+
+// moe_route: one warp per token.
+__global__ void __launch_bounds__(kThreads)
+    moe_route_kernel(const float* __restrict__ logits, int32_t* __restrict__ ids,
+                     float* __restrict__ wts, int B, int E, int top_k) {
+  const int t = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (t >= B) return;
+  const int lane = threadIdx.x & 31;
+  int id;
+  float w;
+  warp_route(logits + (size_t)t * E, E, top_k, id, w);
+  if (lane < top_k) {
+    ids[(size_t)t * top_k + lane] = id;
+    wts[(size_t)t * top_k + lane] = w;
+  }
+}
+
 // Sum each of the V (a power of two, <= 32) values of v over the 32 lanes of
 // the warp with one transposing butterfly: at every step a lane keeps half
 // of its values and receives its partner's partial sums of that half, so the
@@ -273,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                        const uint8_t* __restrict__ gu_scales,
                        const uint16_t* __restrict__ x, const int32_t* __restrict__ ids,
                        uint16_t* __restrict__ h, int32_t* __restrict__ err, int H, int I,
-                       int E, int top_k) {
+                       int E, int top_k, RouteArgs route) {
   extern __shared__ uint4 xs[];
   __shared__ float red[kWarpsPerCta];
   const int lane = threadIdx.x & 31;
@@ -287,7 +365,20 @@ __global__ void __launch_bounds__(kThreads, 3)
   launch_dependents();
 
   // lane s < nslots holds the expert id of slot s; -1 marks "no slot"
-  const int e_lane = (lane < nslots) ? __ldg(ids + (size_t)t * top_k + j0 + lane) : -1;
+  int e_lane;
+  if (route.logits) {  // route the token here, from its logits
+    int rid;
+    float rw;
+    warp_route(route.logits + (size_t)t * E, E, top_k, rid, rw);
+    e_lane = __shfl_sync(0xFFFFFFFFu, rid, lane < nslots ? j0 + lane : 0);
+    if (lane >= nslots) e_lane = -1;
+    if (route.ids_out && j0 == 0 && blockIdx.y == 0 && threadIdx.x < top_k) {
+      route.ids_out[(size_t)t * top_k + lane] = rid;
+      route.w_out[(size_t)t * top_k + lane] = rw;
+    }
+  } else {
+    e_lane = (lane < nslots) ? __ldg(ids + (size_t)t * top_k + j0 + lane) : -1;
+  }
 
   auto load_unit = [&](int s, int seg, GateUpUnit& U) {
     const int e = __shfl_sync(0xFFFFFFFFu, e_lane, s);
@@ -382,7 +473,8 @@ __global__ void __launch_bounds__(kThreads, OPW >= 8 ? 2 : 3)
     moe_down_kernel(const uint8_t* __restrict__ d_codes, const uint8_t* __restrict__ d_scales,
                     const uint16_t* __restrict__ h, const int32_t* __restrict__ ids,
                     const float* __restrict__ wts, float* __restrict__ y,
-                    int32_t* __restrict__ err, int H, int I, int E, int top_k) {
+                    int32_t* __restrict__ err, int H, int I, int E, int top_k,
+                    const float* __restrict__ logits) {
   extern __shared__ uint4 dyn[];
   __shared__ float red[kWarpsPerCta];
   const int lane = threadIdx.x & 31;
@@ -435,10 +527,22 @@ __global__ void __launch_bounds__(kThreads, OPW >= 8 ? 2 : 3)
   // waiting for the intermediate.
   int ja = lane / nblk, ba = lane - (lane / nblk) * nblk;  // this lane's first unit
   DownUnit<OPW> U;
-  if (lane < units) load_unit(__ldg(ids + (size_t)t * top_k + ja), ba, U);
-  for (int j = threadIdx.x; j < top_k; j += kThreads) {
-    s_ids[j] = __ldg(ids + (size_t)t * top_k + j);
-    s_w[j] = __ldg(wts + (size_t)t * top_k + j);
+  if (logits) {  // route the token here, from its logits (same result as gate_up)
+    int rid;
+    float rw;
+    warp_route(logits + (size_t)t * E, E, top_k, rid, rw);
+    const int e0 = __shfl_sync(0xFFFFFFFFu, rid, ja < top_k ? ja : 0);
+    if (lane < units) load_unit(e0, ba, U);
+    if (threadIdx.x < top_k) {
+      s_ids[threadIdx.x] = rid;
+      s_w[threadIdx.x] = rw;
+    }
+  } else {
+    if (lane < units) load_unit(__ldg(ids + (size_t)t * top_k + ja), ba, U);
+    for (int j = threadIdx.x; j < top_k; j += kThreads) {
+      s_ids[j] = __ldg(ids + (size_t)t * top_k + j);
+      s_w[j] = __ldg(wts + (size_t)t * top_k + j);
+    }
   }
   wait_prerequisite();  // the intermediate h is complete from here on
   const int sigma = stage_activations(h + (size_t)t * top_k * I, top_k, I, hs, red);
@@ -545,35 +649,35 @@ int pick_opw(int B, int H, int I) {
 template <int SPW, int NSEG, bool FULL>
 moe_status launch_gate_up(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                           const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
-                          cudaStream_t st) {
+                          cudaStream_t st, RouteArgs route) {
   const size_t smem = (size_t)s->H * 2;
   moe_status rc = allow_smem(moe_gate_up_kernel<SPW, NSEG, FULL>, smem);
   if (rc != MOE_OK) return rc;
   const int groups = (s->top_k + SPW - 1) / SPW;
   const dim3 grid((unsigned)(B * groups), (unsigned)(s->I / kWarpsPerCta));
   moe_gate_up_kernel<SPW, NSEG, FULL><<<grid, kThreads, smem, st>>>(
-      w->gu_codes, w->gu_scales, x, ids, h, err, s->H, s->I, s->E, s->top_k);
+      w->gu_codes, w->gu_scales, x, ids, h, err, s->H, s->I, s->E, s->top_k, route);
   return MOE_OK;
 }
 
 template <int SPW, int NSEG>
 moe_status launch_gate_up_full(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                                const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
-                               cudaStream_t st) {
+                               cudaStream_t st, RouteArgs route) {
   if ((s->H >> 5) % kSegBlocks == 0)
-    return launch_gate_up<SPW, NSEG, true>(s, w, x, ids, B, h, err, st);
-  return launch_gate_up<SPW, NSEG, false>(s, w, x, ids, B, h, err, st);
+    return launch_gate_up<SPW, NSEG, true>(s, w, x, ids, B, h, err, st, route);
+  return launch_gate_up<SPW, NSEG, false>(s, w, x, ids, B, h, err, st, route);
 }
 
 template <int NSEG>
 moe_status launch_gate_up_spw(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                               const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
-                              cudaStream_t st) {
+                              cudaStream_t st, RouteArgs route) {
   switch (pick_spw(B, s->top_k, s->I)) {
-    case 8: return launch_gate_up_full<8, NSEG>(s, w, x, ids, B, h, err, st);
-    case 4: return launch_gate_up_full<4, NSEG>(s, w, x, ids, B, h, err, st);
-    case 2: return launch_gate_up_full<2, NSEG>(s, w, x, ids, B, h, err, st);
-    default: return launch_gate_up_full<1, NSEG>(s, w, x, ids, B, h, err, st);
+    case 8: return launch_gate_up_full<8, NSEG>(s, w, x, ids, B, h, err, st, route);
+    case 4: return launch_gate_up_full<4, NSEG>(s, w, x, ids, B, h, err, st, route);
+    case 2: return launch_gate_up_full<2, NSEG>(s, w, x, ids, B, h, err, st, route);
+    default: return launch_gate_up_full<1, NSEG>(s, w, x, ids, B, h, err, st, route);
   }
 }
 
@@ -583,7 +687,7 @@ moe_status launch_gate_up_spw(const moe_shape* s, const moe_weights* w, const ui
 template <int OPW>
 moe_status launch_down(const moe_shape* s, const moe_weights* w, const uint16_t* h,
                        const int32_t* ids, const float* wts, int32_t B, float* y, int32_t* err,
-                       cudaStream_t st, bool dependent) {
+                       cudaStream_t st, bool dependent, const float* logits) {
   const size_t smem = (size_t)s->top_k * s->I * 2 + (size_t)s->top_k * 8;
   moe_status rc = allow_smem(moe_down_kernel<OPW>, smem);
   if (rc != MOE_OK) return rc;
@@ -598,7 +702,7 @@ moe_status launch_down(const moe_shape* s, const moe_weights* w, const uint16_t*
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_down_kernel<OPW>, w->d_codes, w->d_scales, h,
-                                           ids, wts, y, err, s->H, s->I, s->E, s->top_k);
+                                           ids, wts, y, err, s->H, s->I, s->E, s->top_k, logits);
   if (e != cudaSuccess) {
     set_error("moe_down launch", e);
     return MOE_ERR_CUDA;
@@ -616,44 +720,61 @@ moe_status launch_status(const char* what) {
   return MOE_OK;
 }
 
+// Checks of the routed entry points: the warp router handles E <= 256 and
+// top_k <= 32; logits are FP32 [B][E], 4-byte aligned.
+moe_status check_route(const moe_shape* s, const float* logits) {
+  if (!logits) return MOE_ERR_NULL;
+  if (s->E > kRouteMaxE || s->top_k > 32) {
+    set_error_msg("routing on the device needs E <= 256 and top_k <= 32");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (!aligned(logits, 4)) {
+    set_error_msg("alignment: logits need 4 bytes");
+    return MOE_ERR_ALIGN;
+  }
+  return MOE_OK;
+}
+
+constexpr RouteArgs kNoRoute = {nullptr, nullptr, nullptr};
+
 moe_status gate_up_impl(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                         const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
-                        cudaStream_t st) {
+                        cudaStream_t st, RouteArgs route = kNoRoute) {
   moe_status rc = check_shape(s, B);
   if (rc != MOE_OK) return rc;
   if ((rc = check_weights(w, true, false)) != MOE_OK) return rc;
   if (B == 0) return MOE_OK;
-  if (!x || !ids || !h) return MOE_ERR_NULL;
+  if (!x || (!ids && !route.logits) || !h) return MOE_ERR_NULL;
   if (!aligned(x, 16) || !aligned(h, 16) || !aligned(ids, 4) || !aligned(err, 4)) {
     set_error_msg("alignment: x and h need 16 bytes, ids and err_flag 4");
     return MOE_ERR_ALIGN;
   }
   const int nseg = ((s->H >> 5) + kSegBlocks - 1) / kSegBlocks;  // 2048-element row segments
-  if (nseg == 1) rc = launch_gate_up_spw<1>(s, w, x, ids, B, h, err, st);
-  else if (nseg == 2) rc = launch_gate_up_spw<2>(s, w, x, ids, B, h, err, st);
-  else rc = launch_gate_up_spw<4>(s, w, x, ids, B, h, err, st);
+  if (nseg == 1) rc = launch_gate_up_spw<1>(s, w, x, ids, B, h, err, st, route);
+  else if (nseg == 2) rc = launch_gate_up_spw<2>(s, w, x, ids, B, h, err, st, route);
+  else rc = launch_gate_up_spw<4>(s, w, x, ids, B, h, err, st, route);
   if (rc != MOE_OK) return rc;
   return launch_status("moe_gate_up launch");
 }
 
 moe_status down_impl(const moe_shape* s, const moe_weights* w, const uint16_t* h,
                      const int32_t* ids, const float* wts, int32_t B, float* y, int32_t* err,
-                     cudaStream_t st, bool dependent) {
+                     cudaStream_t st, bool dependent, const float* logits = nullptr) {
   moe_status rc = check_shape(s, B);
   if (rc != MOE_OK) return rc;
   if ((rc = check_weights(w, false, true)) != MOE_OK) return rc;
   if (B == 0) return MOE_OK;
-  if (!h || !ids || !wts || !y) return MOE_ERR_NULL;
+  if (!h || ((!ids || !wts) && !logits) || !y) return MOE_ERR_NULL;
   if (!aligned(h, 16) || !aligned(ids, 4) || !aligned(wts, 4) || !aligned(y, 4) ||
       !aligned(err, 4)) {
     set_error_msg("alignment: h needs 16 bytes, ids/wts/y/err_flag 4");
     return MOE_ERR_ALIGN;
   }
   switch (pick_opw(B, s->H, s->I)) {
-    case 8: rc = launch_down<8>(s, w, h, ids, wts, B, y, err, st, dependent); break;
-    case 4: rc = launch_down<4>(s, w, h, ids, wts, B, y, err, st, dependent); break;
-    case 2: rc = launch_down<2>(s, w, h, ids, wts, B, y, err, st, dependent); break;
-    default: rc = launch_down<1>(s, w, h, ids, wts, B, y, err, st, dependent); break;
+    case 8: rc = launch_down<8>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
+    case 4: rc = launch_down<4>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
+    case 2: rc = launch_down<2>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
+    default: rc = launch_down<1>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
   }
   if (rc != MOE_OK) return rc;
   return launch_status("moe_down launch");
@@ -686,6 +807,45 @@ extern "C" moe_status moe_layer(const moe_shape* shape, const moe_weights* w, co
   rc = gate_up_impl(shape, w, x, ids, B, h_scratch, err_flag, (cudaStream_t)stream);
   if (rc != MOE_OK) return rc;
   return down_impl(shape, w, h_scratch, ids, wts, B, y, err_flag, (cudaStream_t)stream, true);
+}
+
+extern "C" moe_status moe_route(const moe_shape* shape, const float* logits, int32_t B,
+                                int32_t* ids, float* wts, void* stream) {
+  moe_status rc = check_shape(shape, B);
+  if (rc != MOE_OK) return rc;
+  if ((rc = check_route(shape, logits)) != MOE_OK) return rc;
+  if (B == 0) return MOE_OK;
+  if (!ids || !wts) return MOE_ERR_NULL;
+  if (!aligned(ids, 4) || !aligned(wts, 4)) {
+    set_error_msg("alignment: ids and wts need 4 bytes");
+    return MOE_ERR_ALIGN;
+  }
+  const unsigned grid = (unsigned)((B + kWarpsPerCta - 1) / kWarpsPerCta);
+  moe_route_kernel<<<grid, kThreads, 0, (cudaStream_t)stream>>>(logits, ids, wts, B, shape->E,
+                                                               shape->top_k);
+  return launch_status("moe_route launch");
+}
+
+extern "C" moe_status moe_layer_routed(const moe_shape* shape, const moe_weights* w,
+                                       const uint16_t* x, const float* logits, int32_t B,
+                                       uint16_t* h_scratch, float* y, int32_t* ids_out,
+                                       float* wts_out, int32_t* err_flag, void* stream) {
+  moe_status rc = check_shape(shape, B);
+  if (rc != MOE_OK) return rc;
+  if ((rc = check_weights(w, true, true)) != MOE_OK) return rc;
+  if ((rc = check_route(shape, logits)) != MOE_OK) return rc;
+  if (B == 0) return MOE_OK;
+  if (!x || !h_scratch || !y) return MOE_ERR_NULL;
+  if ((ids_out == nullptr) != (wts_out == nullptr)) return MOE_ERR_NULL;
+  if (!aligned(ids_out, 4) || !aligned(wts_out, 4)) {
+    set_error_msg("alignment: ids_out and wts_out need 4 bytes");
+    return MOE_ERR_ALIGN;
+  }
+  const RouteArgs route = {logits, ids_out, wts_out};
+  rc = gate_up_impl(shape, w, x, nullptr, B, h_scratch, err_flag, (cudaStream_t)stream, route);
+  if (rc != MOE_OK) return rc;
+  return down_impl(shape, w, h_scratch, nullptr, nullptr, B, y, err_flag, (cudaStream_t)stream,
+                   true, logits);
 }
 
 extern "C" moe_status moe_layer_host(const moe_shape* shape, const moe_weights* w,

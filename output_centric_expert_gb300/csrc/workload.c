@@ -128,3 +128,16 @@ int wl_route(uint64_t logit_key, uint64_t bias_key, double bias_std, int32_t B,
   free(taken);
   return 0;
 }
+
+/* The router logits wl_route draws, as FP32 [B][E] (for a router run by the
+ * caller): logits[b,e] = (float)(normal(logit_key, b*E + e)
+ *                                + bias_std * normal(bias_key, e)). */
+void wl_logits(uint64_t logit_key, uint64_t bias_key, double bias_std, int32_t B, int32_t E,
+               float* out) {
+  for (int32_t b = 0; b < B; ++b)
+    for (int32_t e = 0; e < E; ++e) {
+      double l = wl_normal_at(logit_key, (uint64_t)b * (uint64_t)E + (uint64_t)e);
+      if (bias_std != 0.0) l += bias_std * wl_normal_at(bias_key, (uint64_t)e);
+      out[(size_t)b * E + e] = (float)l;
+    }
+}

@@ -57,6 +57,10 @@ def lib() -> ctypes.CDLL:
         L.moe_down.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp]
         L.moe_layer.restype = ctypes.c_int
         L.moe_layer.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp, vp]
+        L.moe_route.restype = ctypes.c_int
+        L.moe_route.argtypes = [sp, vp, i32, vp, vp, vp]
+        L.moe_layer_routed.restype = ctypes.c_int
+        L.moe_layer_routed.argtypes = [sp, wp, vp, vp, i32, vp, vp, vp, vp, vp, vp]
         L.moe_layer_noalloc.restype = ctypes.c_int
         L.moe_layer_noalloc.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp]
         L.moe_layer_host.restype = ctypes.c_int
@@ -199,6 +203,31 @@ def moe_layer(weights: DeviceWeights, x: torch.Tensor, ids: torch.Tensor, wts: t
     return y
 
 
+def moe_route(shape: MoeShape, logits: torch.Tensor, ids: torch.Tensor, wts: torch.Tensor,
+              stream=None):
+    """ids[B,k], wts[B,k] = top-k routing of FP32 logits [B,E] (on the device)."""
+    B = logits.shape[0]
+    _check("moe_route", lib().moe_route(
+        ctypes.byref(shape), _ptr(logits, (torch.float32,), "logits"), B,
+        _ptr(ids, (torch.int32,), "ids"), _ptr(wts, (torch.float32,), "wts"), _stream(stream)))
+    return ids, wts
+
+
+def moe_layer_routed(weights: DeviceWeights, x: torch.Tensor, logits: torch.Tensor,
+                     h_scratch: torch.Tensor, y: torch.Tensor, ids_out: torch.Tensor | None = None,
+                     wts_out: torch.Tensor | None = None, err_flag: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """The layer from router logits (both kernels route each token themselves)."""
+    B = x.shape[0]
+    _check("moe_layer_routed", lib().moe_layer_routed(
+        ctypes.byref(weights.shape), ctypes.byref(weights.struct), _ptr(x, _BF16, "x"),
+        _ptr(logits, (torch.float32,), "logits"), B, _ptr(h_scratch, _BF16, "h_scratch"),
+        _ptr(y, (torch.float32,), "y"), _ptr(ids_out, (torch.int32,), "ids_out"),
+        _ptr(wts_out, (torch.float32,), "wts_out"), _ptr(err_flag, (torch.int32,), "err_flag"),
+        _stream(stream)))
+    return y
+
+
 def moe_layer_noalloc(weights: DeviceWeights, x: torch.Tensor, ids: torch.Tensor,
                       wts: torch.Tensor, y: torch.Tensor, err_flag: torch.Tensor | None = None,
                       stream=None) -> torch.Tensor:
@@ -240,4 +269,5 @@ def moe_layer_host(weights: DeviceWeights, x_host: torch.Tensor, ids_host: torch
 def exported_symbols() -> list[str]:
     """The entry points include/warp_decode.h declares."""
     return ["moe_packed_bytes", "moe_pack_weights", "moe_gate_up", "moe_down", "moe_layer",
-            "moe_layer_host", "moe_layer_noalloc", "moe_status_string", "moe_last_error"]
+            "moe_layer_host", "moe_layer_noalloc", "moe_route", "moe_layer_routed",
+            "moe_status_string", "moe_last_error"]

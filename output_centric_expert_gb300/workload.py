@@ -108,6 +108,8 @@ def _lib() -> ctypes.CDLL:
         lib.wl_normal_f32.argtypes = [u64, u64, u64, ctypes.c_double, ctypes.c_double, ctypes.c_void_p]
         lib.wl_normal_bf16.restype = None
         lib.wl_normal_bf16.argtypes = [u64, u64, u64, ctypes.c_void_p]
+        lib.wl_logits.restype = None
+        lib.wl_logits.argtypes = [u64, u64, ctypes.c_double, i32, i32, ctypes.c_void_p]
         lib.wl_route.restype = ctypes.c_int
         lib.wl_route.argtypes = [u64, u64, ctypes.c_double, i32, i32, i32, ctypes.c_void_p, ctypes.c_void_p]
         lib._wl_typed = True
@@ -186,6 +188,20 @@ def tokens(shape: LayerShape, B: int, seed: int = 0, batch: int = 0, routing: st
     if rc != 0:
         raise ValueError("wl_route rejected its arguments")
     return x, ids, w
+
+
+def logits(shape: LayerShape, B: int, seed: int = 0, batch: int = 0, routing: str = "uniform"):
+    """The router logits of the same decode step as tokens(), as float32 [B,E]
+    (for a router that runs on the device instead of in the generator)."""
+    if routing not in ("uniform", "skewed"):
+        raise ValueError(f"unknown routing {routing!r}")
+    lib = _lib()
+    out = np.empty((B, shape.E), dtype=np.float32)
+    if B:
+        lib.wl_logits(lib.wl_stream_key(seed, _token_stream(_STREAM_LOGITS, batch)),
+                      lib.wl_stream_key(seed, _weight_stream(_STREAM_BIAS, 0)),
+                      SKEW_BIAS_STD if routing == "skewed" else 0.0, B, shape.E, out.ctypes.data)
+    return out
 
 
 def bf16_bits_to_f32(x_bits: np.ndarray) -> np.ndarray:

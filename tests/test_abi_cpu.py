@@ -65,6 +65,20 @@ def test_host_validation_rejects_before_launch():
     assert ops.status_string(2) == "unsupported shape"
 
 
+def test_routed_entry_points_validate_before_launch():
+    L = ops.lib()
+    P = 0x20000
+    w = _fake_weights()
+    ok = ops.make_shape(2048, 768, 128, 8)
+    assert L.moe_route(ctypes.byref(ok), None, 4, P, P, None) == 1          # no logits
+    assert L.moe_route(ctypes.byref(ops.make_shape(2048, 768, 512, 8)), P, 4, P, P, None) == 5  # E > 256
+    assert L.moe_route(ctypes.byref(ops.make_shape(2048, 768, 128, 40)), P, 4, P, P, None) == 5  # k > 32
+    assert L.moe_route(ctypes.byref(ok), P + 2, 4, P, P, None) == 3         # misaligned logits
+    assert L.moe_route(ctypes.byref(ok), P, 0, None, None, None) == 0       # empty batch
+    assert L.moe_layer_routed(ctypes.byref(ok), ctypes.byref(w), P, P, 4, P, P, P, None, None, None) == 1
+    assert L.moe_layer_routed(ctypes.byref(ok), ctypes.byref(w), P, None, 4, P, P, None, None, None, None) == 1
+
+
 def test_packed_sizes():
     q30 = ops.make_shape(2048, 768, 128, 8)
     sizes = [ops.moe_packed_bytes(q30, w) for w in range(4)]

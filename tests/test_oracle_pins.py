@@ -376,3 +376,27 @@ def test_buffer_arithmetic_from_the_pages():
     q30 = workload.SHAPES["q30"]
     assert q30.top_k == g["experts"] and q30.H == g["hidden"]
     assert q30.top_k * q30.H * g["bytes_per_element"] == g["value"] == 32 * 1024
+
+
+# ------------------------------------------------------------------ router --
+
+def test_router_matches_torch_softmax_topk():
+    """Distinct logits: oracle.route == torch softmax (float64) + topk + renorm."""
+    rng = np.random.default_rng(7)
+    L = rng.standard_normal((20, 64)).astype(np.float32)
+    ids, w = oracle.route(L, 6)
+    p = torch.softmax(torch.from_numpy(L.astype(np.float64)), dim=1)
+    pv, pi = torch.topk(p, 6, dim=1)
+    assert np.array_equal(ids, pi.numpy().astype(np.int32))
+    np.testing.assert_allclose(w, (pv / pv.sum(dim=1, keepdim=True)).numpy(), rtol=1e-14)
+
+
+def test_router_ties_and_special_cases():
+    L = np.array([[1.0, 3.0, 3.0, 0.5, 3.0]], np.float32)
+    ids, w = oracle.route(L, 3)
+    assert ids.tolist() == [[1, 2, 4]]  # equal logits: lower index first
+    np.testing.assert_allclose(w, [[1 / 3, 1 / 3, 1 / 3]], rtol=1e-15)
+    ids, w = oracle.route(L, 1)  # top-1: weight exactly 1
+    assert ids.tolist() == [[1]] and w.tolist() == [[1.0]]
+    ids, w = oracle.route(np.zeros((1, 4), np.float32), 4)  # k = E, all equal
+    assert ids.tolist() == [[0, 1, 2, 3]] and np.allclose(w, 0.25)
