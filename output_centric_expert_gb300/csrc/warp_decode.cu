@@ -468,8 +468,11 @@ struct DownUnit {
   uint32_t s[OPW];
 };
 
-template <int OPW>
-__global__ void __launch_bounds__(kThreads, OPW >= 8 ? 2 : 3)
+// UPL: units each lane requests at once. When the whole grid fits on the GPU
+// in one wave (small batches), a lane with one output has registers to keep
+// UPL of its (slot, block) units in flight instead of one HBM round trip each.
+template <int OPW, int UPL>
+__global__ void __launch_bounds__(kThreads, (OPW * UPL >= 8) ? 2 : 3)
     moe_down_kernel(const uint8_t* __restrict__ d_codes, const uint8_t* __restrict__ d_scales,
                     const uint16_t* __restrict__ h, const int32_t* __restrict__ ids,
                     const float* __restrict__ wts, float* __restrict__ y,
@@ -513,32 +516,46 @@ __global__ void __launch_bounds__(kThreads, OPW >= 8 ? 2 : 3)
     for (int r = 0; r < OPW; ++r)
       acc[r] = fmaf(block_dot(a, U.c[r]), e8m0_to_f32(U.s[r]) * wj, acc[r]);
   };
-  // (slot, block) of a unit, advanced by 32 units (one lane stride)
-  auto advance = [&](int& jj, int& bb) {
-    bb += 32;
-    while (bb >= nblk) {
-      bb -= nblk;
-      ++jj;
-    }
+  // (slot, block) of a unit, advanced by `step` units
+  auto advance = [&](int& jj, int& bb, int step) {
+    bb += step;
+    const int q = bb / nblk;
+    jj += q;
+    bb -= q * nblk;
   };
 
+  // This lane's units are u = lane + 32*(q + UPL*i); a batch holds q < UPL.
+  int jj[UPL], bb[UPL];
+  jj[0] = lane / nblk;
+  bb[0] = lane - jj[0] * nblk;
+#pragma unroll
+  for (int q = 1; q < UPL; ++q) {
+    jj[q] = jj[q - 1];
+    bb[q] = bb[q - 1];
+    advance(jj[q], bb[q], 32);
+  }
+  DownUnit<OPW> U[UPL];
+
   // The ids, routing weights and down weights are inputs of the layer, not
-  // produced by moe_gate_up: this lane's first unit is requested before
-  // waiting for the intermediate.
-  int ja = lane / nblk, ba = lane - (lane / nblk) * nblk;  // this lane's first unit
-  DownUnit<OPW> U;
+  // produced by moe_gate_up: the first batch is requested before waiting for
+  // the intermediate.
   if (logits) {  // route the token here, from its logits (same result as gate_up)
     int rid;
     float rw;
     warp_route(logits + (size_t)t * E, E, top_k, rid, rw);
-    const int e0 = __shfl_sync(0xFFFFFFFFu, rid, ja < top_k ? ja : 0);
-    if (lane < units) load_unit(e0, ba, U);
+#pragma unroll
+    for (int q = 0; q < UPL; ++q) {
+      const int e = __shfl_sync(0xFFFFFFFFu, rid, jj[q] < top_k ? jj[q] : 0);
+      if (lane + 32 * q < units) load_unit(e, bb[q], U[q]);
+    }
     if (threadIdx.x < top_k) {
       s_ids[threadIdx.x] = rid;
       s_w[threadIdx.x] = rw;
     }
   } else {
-    if (lane < units) load_unit(__ldg(ids + (size_t)t * top_k + ja), ba, U);
+#pragma unroll
+    for (int q = 0; q < UPL; ++q)
+      if (lane + 32 * q < units) load_unit(__ldg(ids + (size_t)t * top_k + jj[q]), bb[q], U[q]);
     for (int j = threadIdx.x; j < top_k; j += kThreads) {
       s_ids[j] = __ldg(ids + (size_t)t * top_k + j);
       s_w[j] = __ldg(wts + (size_t)t * top_k + j);
@@ -548,10 +565,15 @@ __global__ void __launch_bounds__(kThreads, OPW >= 8 ? 2 : 3)
   const int sigma = stage_activations(h + (size_t)t * top_k * I, top_k, I, hs, red);
   const float unscale = exp2i(-sigma);
 
-  for (int u0 = lane; u0 < units; u0 += 32) {
-    compute_unit(ja, ba, U);
-    advance(ja, ba);
-    if (u0 + 32 < units) load_unit(s_ids[ja], ba, U);
+  for (int u0 = lane; u0 < units; u0 += 32 * UPL) {
+#pragma unroll
+    for (int q = 0; q < UPL; ++q)
+      if (u0 + 32 * q < units) compute_unit(jj[q], bb[q], U[q]);
+#pragma unroll
+    for (int q = 0; q < UPL; ++q) {
+      advance(jj[q], bb[q], 32 * UPL);
+      if (u0 + 32 * (UPL + q) < units) load_unit(s_ids[jj[q]], bb[q], U[q]);
+    }
   }
   // lane l holds the total of output l / (32 / OPW)
   const float tot = warp_sum_transposed<OPW>(acc) * unscale;
@@ -684,12 +706,12 @@ moe_status launch_gate_up_spw(const moe_shape* s, const moe_weights* w, const ui
 // dependent = true launches moe_down as a programmatic dependent of the kernel
 // before it on the stream (used by moe_layer, where that kernel is moe_gate_up
 // and only h is produced by it).
-template <int OPW>
+template <int OPW, int UPL>
 moe_status launch_down(const moe_shape* s, const moe_weights* w, const uint16_t* h,
                        const int32_t* ids, const float* wts, int32_t B, float* y, int32_t* err,
                        cudaStream_t st, bool dependent, const float* logits) {
   const size_t smem = (size_t)s->top_k * s->I * 2 + (size_t)s->top_k * 8;
-  moe_status rc = allow_smem(moe_down_kernel<OPW>, smem);
+  moe_status rc = allow_smem(moe_down_kernel<OPW, UPL>, smem);
   if (rc != MOE_OK) return rc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)B, (unsigned)(s->H / (kWarpsPerCta * OPW)));
@@ -701,7 +723,7 @@ moe_status launch_down(const moe_shape* s, const moe_weights* w, const uint16_t*
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_down_kernel<OPW>, w->d_codes, w->d_scales, h,
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_down_kernel<OPW, UPL>, w->d_codes, w->d_scales, h,
                                            ids, wts, y, err, s->H, s->I, s->E, s->top_k, logits);
   if (e != cudaSuccess) {
     set_error("moe_down launch", e);
@@ -771,10 +793,17 @@ moe_status down_impl(const moe_shape* s, const moe_weights* w, const uint16_t* h
     return MOE_ERR_ALIGN;
   }
   switch (pick_opw(B, s->H, s->I)) {
-    case 8: rc = launch_down<8>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
-    case 4: rc = launch_down<4>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
-    case 2: rc = launch_down<2>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
-    default: rc = launch_down<1>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
+    case 8: rc = launch_down<8, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
+    case 4: rc = launch_down<4, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
+    case 2: rc = launch_down<2, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
+    default:
+      // one output per warp: batch 8 units per lane when the grid is one wave
+      // at 2 CTAs per SM
+      if ((int64_t)B * (s->H / kWarpsPerCta) <= 2 * 152)
+        rc = launch_down<1, 8>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+      else
+        rc = launch_down<1, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+      break;
   }
   if (rc != MOE_OK) return rc;
   return launch_status("moe_down launch");
