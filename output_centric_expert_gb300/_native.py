@@ -3,8 +3,10 @@
 Two shared libraries are built from ``csrc/``:
 
 * ``libwarp_decode.so`` -- the C-ABI library: the two CUDA kernels
-  (``moe_gate_up``, ``moe_down``), their launchers and the host-side MXFP8
-  packer. Compiled by ``nvcc`` for sm_103a only.
+  (``moe_gate_up`` in wd_gate_up*.cu, ``moe_down`` in wd_down.cu), the C-ABI
+  entry points and router (warp_decode.cu) and the host-side MXFP8 packer.
+  Compiled by ``nvcc`` for sm_103a only, one translation unit per file, in
+  parallel.
 * ``libworkload.so`` -- the seeded synthetic input generator (plain C, gcc).
 
 Nothing here falls back to another implementation: if a library is missing or
@@ -55,7 +57,7 @@ def _stale(target: str, sources: list[str]) -> bool:
 
 
 def _cuda_sources() -> list[str]:
-    names = ["warp_decode.cu", "pack.cpp"]
+    names = ["warp_decode.cu", "wd_gate_up.cu", "wd_gate_up_fixed.cu", "wd_down.cu", "pack.cpp"]
     return [os.path.join(CSRC, n) for n in names]
 
 

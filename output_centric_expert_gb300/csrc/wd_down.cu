@@ -1,0 +1,224 @@
+// moe_down: the second kernel of the layer and its launcher.
+#include "wd_device.cuh"
+
+namespace wd {
+namespace {
+
+// --------------------------------------------------------------- moe_down --
+// grid.x = B (token), grid.y = H / (8*OPW) (output block); 8 warps, warp w owns
+// outputs o0 .. o0+OPW-1 with o0 = (8*blockIdx.y + w) * OPW. Dynamic shared
+// memory: the token's top_k intermediates as scaled f16 (top_k * I), plus
+// the token's ids and routing weights.
+//
+// A warp's top_k * I/32 (slot, block) units are spread over its lanes; every
+// unit multiplies one block of the intermediate (read once from shared memory)
+// with the same block of the OPW down rows, and adds partial * scale * w[slot]
+// into the lane's OPW FP32 accumulators -- the routing weight is folded into
+// the sum, so no per-expert output exists.
+
+template <int OPW>
+struct DownUnit {
+  Codes32 c[OPW];
+  uint32_t s[OPW];
+};
+
+// UPL: units each lane requests at once. When the whole grid fits on the GPU
+// in one wave (small batches), a lane with one output has registers to keep
+// UPL of its (slot, block) units in flight instead of one HBM round trip each.
+// KI: the row length I fixed at compile time (0: taken from the argument). With
+// it the row strides are constants the loads take as immediates, and the
+// (slot, block) advance divides by a constant.
+template <int OPW, int UPL, int KI>
+__global__ void __launch_bounds__(kThreads, (OPW * UPL >= 8) ? 2 : 3)
+    moe_down_kernel(const uint8_t* __restrict__ d_codes, const uint8_t* __restrict__ d_scales,
+                    const uint16_t* __restrict__ h, const int32_t* __restrict__ ids,
+                    const float* __restrict__ wts, float* __restrict__ y,
+                    int32_t* __restrict__ err, int H, int I_arg, int E, int top_k,
+                    const float* __restrict__ logits) {
+  const int I = KI ? KI : I_arg;
+  extern __shared__ uint4 dyn[];
+  __shared__ float red[kWarpsPerCta];
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x;
+  const int o0 = (blockIdx.y * kWarpsPerCta + (threadIdx.x >> 5)) * OPW;
+  const int nblk = I >> 5;
+  uint4* hs = dyn;                                                      // top_k*I/8 uint4
+  int* s_ids = reinterpret_cast<int*>(dyn + (size_t)top_k * (I >> 3));  // top_k
+  float* s_w = reinterpret_cast<float*>(s_ids + top_k);                 // top_k
+
+  const int units = top_k * nblk;
+  float acc[OPW];
+#pragma unroll
+  for (int r = 0; r < OPW; ++r) acc[r] = 0.0f;
+  bool bad = false;
+
+  auto load_unit = [&](int e, int bb, DownUnit<OPW>& U) {
+    if (e < 0 || e >= E) return;
+#pragma unroll
+    for (int r = 0; r < OPW; ++r) {
+      const size_t row = (size_t)e * H + o0 + r;
+      U.c[r] = ld_codes32(d_codes + row * I + (size_t)bb * 32);
+      U.s[r] = __ldg(d_scales + row * nblk + bb);
+    }
+  };
+  auto compute_unit = [&](int jj, int bb, const DownUnit<OPW>& U) {
+    const int e = s_ids[jj];
+    if (e < 0 || e >= E) {
+      bad = true;
+      return;
+    }
+    const float wj = s_w[jj];
+    uint32_t a[16];
+    ld_act_block(hs + (size_t)jj * (I >> 3), nblk, bb, a);
+#pragma unroll
+    for (int r = 0; r < OPW; ++r)
+      acc[r] = fmaf(block_dot(a, U.c[r]), e8m0_to_f32(U.s[r]) * wj, acc[r]);
+  };
+  // (slot, block) of a unit, advanced by `step` units
+  auto advance = [&](int& jj, int& bb, int step) {
+    bb += step;
+    const int q = bb / nblk;
+    jj += q;
+    bb -= q * nblk;
+  };
+
+  // This lane's units are u = lane + 32*(q + UPL*i); a batch holds q < UPL.
+  int jj[UPL], bb[UPL];
+  jj[0] = lane / nblk;
+  bb[0] = lane - jj[0] * nblk;
+#pragma unroll
+  for (int q = 1; q < UPL; ++q) {
+    jj[q] = jj[q - 1];
+    bb[q] = bb[q - 1];
+    advance(jj[q], bb[q], 32);
+  }
+  DownUnit<OPW> U[UPL];
+
+  // The ids, routing weights and down weights are inputs of the layer, not
+  // produced by moe_gate_up: the first batch is requested before waiting for
+  // the intermediate.
+  if (logits) {  // route the token here, from its logits (same result as gate_up)
+    int rid;
+    float rw;
+    warp_route(logits + (size_t)t * E, E, top_k, rid, rw);
+#pragma unroll
+    for (int q = 0; q < UPL; ++q) {
+      const int e = __shfl_sync(0xFFFFFFFFu, rid, jj[q] < top_k ? jj[q] : 0);
+      if (lane + 32 * q < units) load_unit(e, bb[q], U[q]);
+    }
+    if (threadIdx.x < top_k) {
+      s_ids[threadIdx.x] = rid;
+      s_w[threadIdx.x] = rw;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < UPL; ++q)
+      if (lane + 32 * q < units) load_unit(__ldg(ids + (size_t)t * top_k + jj[q]), bb[q], U[q]);
+    for (int j = threadIdx.x; j < top_k; j += kThreads) {
+      s_ids[j] = __ldg(ids + (size_t)t * top_k + j);
+      s_w[j] = __ldg(wts + (size_t)t * top_k + j);
+    }
+  }
+  wait_prerequisite();  // the intermediate h is complete from here on
+  const int sigma = stage_activations(h + (size_t)t * top_k * I, top_k, I, hs, red);
+  const float unscale = exp2i(-sigma);
+
+  for (int u0 = lane; u0 < units; u0 += 32 * UPL) {
+#pragma unroll
+    for (int q = 0; q < UPL; ++q)
+      if (u0 + 32 * q < units) compute_unit(jj[q], bb[q], U[q]);
+#pragma unroll
+    for (int q = 0; q < UPL; ++q) {
+      advance(jj[q], bb[q], 32 * UPL);
+      if (u0 + 32 * (UPL + q) < units) load_unit(s_ids[jj[q]], bb[q], U[q]);
+    }
+  }
+  // lane l holds the total of output l / (32 / OPW)
+  const float tot = warp_sum_transposed<OPW>(acc) * unscale;
+  if (bad) flag_invalid(err);
+  if (lane % (32 / OPW) == 0) y[(size_t)t * H + o0 + lane / (32 / OPW)] = tot;
+}
+
+// Outputs per warp of moe_down: 8 for rows of at most 1024 elements when at
+// least 6 CTAs per SM remain (measured faster there), else as many as keep
+// at least kMinCtas CTAs.
+int pick_opw(int B, int H, int I) {
+  if (I <= 1024 && (int64_t)B * (H / (kWarpsPerCta * 8)) >= 6 * 152) return 8;
+  const int opws[3] = {4, 2, 1};
+  for (int v : opws) {
+    const int64_t ctas = (int64_t)B * (H / (kWarpsPerCta * v));
+    if (ctas >= kMinCtas) return v;
+  }
+  return 1;
+}
+
+template <int OPW, int UPL, int KI>
+moe_status launch_down_ki(const moe_shape* s, const moe_weights* w, const uint16_t* h,
+                          const int32_t* ids, const float* wts, int32_t B, float* y, int32_t* err,
+                          cudaStream_t st, bool dependent, const float* logits) {
+  const size_t smem = (size_t)s->top_k * s->I * 2 + (size_t)s->top_k * 8;
+  moe_status rc = allow_smem(moe_down_kernel<OPW, UPL, KI>, smem);
+  if (rc != MOE_OK) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)B, (unsigned)(s->H / (kWarpsPerCta * OPW)));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_down_kernel<OPW, UPL, KI>, w->d_codes,
+                                           w->d_scales, h, ids, wts, y, err, s->H, s->I, s->E,
+                                           s->top_k, logits);
+  if (e != cudaSuccess) {
+    set_error("moe_down launch", e);
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+// Row lengths with their own compiled kernel: the intermediate sizes of the
+// Qwen3-30B-A3B-, Qwen3-235B-A22B- and DeepSeek-V3-shaped layers (8 outputs
+// per warp is only chosen for I <= 1024); every other I runs the kernel that
+// reads I at run time.
+template <int OPW, int UPL>
+moe_status launch_down(const moe_shape* s, const moe_weights* w, const uint16_t* h,
+                       const int32_t* ids, const float* wts, int32_t B, float* y, int32_t* err,
+                       cudaStream_t st, bool dependent, const float* logits) {
+  if (s->I == 768)
+    return launch_down_ki<OPW, UPL, 768>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+  if constexpr (OPW != 8) {
+    if (s->I == 1536)
+      return launch_down_ki<OPW, UPL, 1536>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+    if (s->I == 2048)
+      return launch_down_ki<OPW, UPL, 2048>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+  }
+  return launch_down_ki<OPW, UPL, 0>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+}
+
+}  // namespace
+
+moe_status launch_down_kernels(const moe_shape* s, const moe_weights* w, const uint16_t* h,
+                               const int32_t* ids, const float* wts, int32_t B, float* y,
+                               int32_t* err, cudaStream_t st, bool dependent,
+                               const float* logits) {
+  moe_status rc;
+  switch (pick_opw(B, s->H, s->I)) {
+    case 8: rc = launch_down<8, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
+    case 4: rc = launch_down<4, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
+    case 2: rc = launch_down<2, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
+    default:
+      // one output per warp: batch 8 units per lane when the grid is one wave
+      // at 2 CTAs per SM
+      if ((int64_t)B * (s->H / kWarpsPerCta) <= 2 * 152)
+        rc = launch_down<1, 8>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+      else
+        rc = launch_down<1, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+      break;
+  }
+  return rc;
+}
+
+}  // namespace wd
