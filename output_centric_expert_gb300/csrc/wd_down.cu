@@ -139,11 +139,14 @@ __global__ void __launch_bounds__(kThreads, (OPW * UPL >= 8) ? 2 : 3)
   if (lane % (32 / OPW) == 0) y[(size_t)t * H + o0 + lane / (32 / OPW)] = tot;
 }
 
-// Outputs per warp of moe_down: 8 for rows of at most 1024 elements when at
-// least 6 CTAs per SM remain (measured faster there), else as many as keep
-// at least kMinCtas CTAs.
+// Outputs per warp of moe_down beyond the single-wave small batches: 8 for
+// rows of at most 1024 elements (measured faster there from B=16 up: Q30
+// B=16 39.5 -> 31.1 us against 2 outputs per warp; slower for the 1536-element
+// rows of the 235B-shaped layer), else as many as keep at least kMinCtas CTAs.
+// A CTA covers 8 * OPW outputs, so OPW = 8 needs H % 64 == 0 (H % 32 == 0 is
+// enough for the others).
 int pick_opw(int B, int H, int I) {
-  if (I <= 1024 && (int64_t)B * (H / (kWarpsPerCta * 8)) >= 6 * 152) return 8;
+  if (H % (kWarpsPerCta * 8) == 0 && I <= 1024) return 8;
   const int opws[3] = {4, 2, 1};
   for (int v : opws) {
     const int64_t ctas = (int64_t)B * (H / (kWarpsPerCta * v));
@@ -204,21 +207,25 @@ moe_status launch_down_kernels(const moe_shape* s, const moe_weights* w, const u
                                const int32_t* ids, const float* wts, int32_t B, float* y,
                                int32_t* err, cudaStream_t st, bool dependent,
                                const float* logits) {
-  moe_status rc;
+  // Small batches: the fewest outputs per warp (OPW) that make the grid a
+  // single wave at 2 CTAs per SM, each lane keeping 8 / OPW units in flight.
+  // Fewer, fuller CTAs stage each token's intermediate fewer times and need
+  // fewer round trips per lane than one-output warps (Q30 B=8: 32.6 -> 18.5 us).
+  const int64_t ctas_opw1 = (int64_t)B * (s->H / kWarpsPerCta);
+  if (ctas_opw1 <= 2 * 152)
+    return launch_down<1, 8>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+  if (ctas_opw1 / 2 <= 2 * 152)
+    return launch_down<2, 4>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+  if (ctas_opw1 / 4 <= 2 * 152)
+    return launch_down<4, 2>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+  if (s->H % (kWarpsPerCta * 8) == 0 && ctas_opw1 / 8 <= 2 * 152)
+    return launch_down<8, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
   switch (pick_opw(B, s->H, s->I)) {
-    case 8: rc = launch_down<8, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
-    case 4: rc = launch_down<4, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
-    case 2: rc = launch_down<2, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits); break;
-    default:
-      // one output per warp: batch 8 units per lane when the grid is one wave
-      // at 2 CTAs per SM
-      if ((int64_t)B * (s->H / kWarpsPerCta) <= 2 * 152)
-        rc = launch_down<1, 8>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
-      else
-        rc = launch_down<1, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
-      break;
+    case 8: return launch_down<8, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+    case 4: return launch_down<4, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+    case 2: return launch_down<2, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+    default: return launch_down<1, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
   }
-  return rc;
 }
 
 }  // namespace wd

@@ -91,7 +91,12 @@ def test_tiny_config_full(tiny):
     _check_h(h, h_ref)
 
 
-@pytest.mark.parametrize("B,routing", [(1, "uniform"), (32, "uniform"), (64, "skewed"), (7, "uniform")])
+# B covers every moe_down configuration the launcher picks for this shape:
+# 1 output x 8 units per lane (B=1), 2 x 4 (B=2), 4 x 2 (B=4, in
+# test_activation_scale_extremes), 8 x 1 as one wave (B=7) and as several
+# waves (B=32, 64).
+@pytest.mark.parametrize("B,routing", [(1, "uniform"), (2, "uniform"), (32, "uniform"), (64, "skewed"),
+                                       (7, "uniform")])
 def test_q30_layer_all_tokens(q30, B, routing):
     """Qwen-3-30B-A3B-shaped layer (H=2048, I=768, E=128, top-8), every token."""
     x, ids, w = workload.tokens(q30.shape, B, routing=routing, batch=B)
@@ -136,15 +141,17 @@ def test_q235_sampled_tokens():
     assert np.all(np.isfinite(y))
 
 
-@pytest.mark.parametrize("name,E,B", [("dsv3", 16, 12), ("mixtral", 8, 6)])
+@pytest.mark.parametrize("name,E,B", [("dsv3", 16, 12), ("mixtral", 8, 6), ("dsv3", 16, 1),
+                                      ("mixtral", 8, 1), ("q235", 8, 1)])
 def test_shape_variants(name, E, B):
     """DeepSeek-V3-shaped (H=7168: partial row segments) and Mixtral-shaped
     (I=14336: a 57 KB intermediate per token) layers, with fewer experts than the
-    models have (parity depends on the row shapes, not on E)."""
+    models have (parity depends on the row shapes, not on E). At B=1 moe_down
+    runs 4 outputs x 2 units (H=7168) or 2 outputs x 4 units (H=4096) per lane."""
     full = workload.SHAPES[name]
     s = workload.LayerShape(full.H, full.I, E, full.top_k)
     x, ids, w = workload.tokens(s, B, batch=11)
-    sample = [0, B // 2, B - 1]
+    sample = sorted({0, B // 2, B - 1})
     layer = Layer(s, oracle_experts=np.unique(ids[sample]))
     y, h = _run_layer(layer, x, ids, w)
     y_ref, h_ref, _ = oracle.moe_layer(layer.ref, x[sample], ids[sample], w[sample], return_h=True)
@@ -165,6 +172,7 @@ def _rand_layer_shape(H, I, E, k, seed=0):
     (96, 160, 5, 3, 5),       # rows shorter than a warp's chunk span
     (544, 64, 3, 3, 2),       # top_k = E
     (256, 128, 8, 8, 4),      # tiny layer with k = E
+    (96, 160, 5, 3, 128),     # H % 64 != 0 where 8 outputs per warp would leave outputs unwritten
 ])
 def test_ragged_and_small_shapes(H, I, E, k, B):
     layer = _rand_layer_shape(H, I, E, k, seed=H + I)
