@@ -92,10 +92,19 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_sha() -> str:
-    src = os.path.join(REPO, "output_centric_expert_gb300", "csrc", "warp_decode.cu")
-    with open(src, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+KERNEL_SOURCES = {
+    "moe_gate_up": ["wd_device.cuh", "wd_gate_up.cuh", "wd_gate_up.cu", "wd_gate_up_fixed.cu"],
+    "moe_down": ["wd_device.cuh", "wd_down.cu"],
+}
+
+
+def kernel_source_sha(kernel: str) -> str:
+    """Hash of the source files that define a kernel and its launch."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(REPO, "output_centric_expert_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str, workload: str):
@@ -107,7 +116,7 @@ def ncu_traffic(kernel: str, workload: str):
     with open(p) as f:
         d = json.load(f)
     ent = d.get(kernel, {}).get(workload)
-    if not ent or ent.get("kernel_sha") != kernel_source_sha():
+    if not ent or ent.get("kernel_sha") != kernel_source_sha(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
