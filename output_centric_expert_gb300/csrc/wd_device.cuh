@@ -66,7 +66,7 @@ struct RouteArgs {
 constexpr RouteArgs kNoRoute = {nullptr, nullptr, nullptr};
 
 // ------------------------------------------------------ host helpers (shared) --
-// Defined in warp_decode.cu; one error message per calling thread.
+// Defined with the C-ABI entry points; one error message per calling thread.
 void set_error(const char* what, cudaError_t e);
 void set_error_msg(const char* msg);
 
