@@ -407,32 +407,52 @@ def run_ours(args, wl, rank, world, local_rank):
     layer_gbs = sum(lay_bytes) / args.steps / (ms_per_step / 1e3) / 1e9
 
     # ---- end to end from pinned host buffers (copies inside the region) ----
+    # Every step copies its x, ids and routing weights in from pinned host
+    # memory and its y back out, through moe_layer_host. value: one stream,
+    # so each step's copies and kernels run in series. pipelined: two streams
+    # take alternate steps with their own buffers, so one step's copies (and
+    # kernels) overlap the other's, as a serving loop with two requests in
+    # flight would run.
     px = [torch.from_numpy(b[0].view(np.int16)).pin_memory() for b in batches]
     pids = [torch.from_numpy(b[1]).pin_memory() for b in batches]
     pw = [torch.from_numpy(b[2]).pin_memory() for b in batches]
-    py = torch.empty((wl.B, s.H), dtype=torch.float32).pin_memory()
-    sx = torch.empty_like(dx[0])
-    sids = torch.empty_like(dids[0])
-    sw = torch.empty_like(dw[0])
+    e2e_streams = [stream, torch.cuda.Stream(device=dev)]
+    e2e_bufs = [{"py": torch.empty((wl.B, s.H), dtype=torch.float32).pin_memory(),
+                 "sx": torch.empty_like(dx[0]), "sids": torch.empty_like(dids[0]),
+                 "sw": torch.empty_like(dw[0]), "h": torch.empty_like(h), "y": torch.empty_like(y)}
+                for _ in e2e_streams]
 
-    def e2e_step(i):
-        b = i % N_BATCHES
-        ops.moe_layer_host(layers[i % N_LAYERS], px[b], pids[b], pw[b], sx, sids, sw, h, y, py,
-                           err, stream)
+    def e2e_step(i, nstreams):
+        b, k = i % N_BATCHES, i % nstreams
+        q = e2e_bufs[k]
+        ops.moe_layer_host(layers[i % N_LAYERS], px[b], pids[b], pw[b], q["sx"], q["sids"], q["sw"],
+                           q["h"], q["y"], q["py"], err, e2e_streams[k])
 
-    for i in range(3):
-        e2e_step(i)
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        e2e_step(i)
-    e1.record(stream)
-    barrier()
+    def e2e_run(nstreams):
+        for i in range(4):
+            e2e_step(i, nstreams)
+        barrier()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(e2e_streams[0])
+        for k in range(1, nstreams):
+            e2e_streams[k].wait_event(t0)
+        for i in range(args.steps):
+            e2e_step(i, nstreams)
+        for k in range(1, nstreams):
+            done = torch.cuda.Event()
+            done.record(e2e_streams[k])
+            e2e_streams[0].wait_event(done)
+        t1.record(e2e_streams[0])
+        barrier()
+        return t0, t1
+
+    p0, p1 = e2e_run(2)
+    e2e_pipe_ms = max_over_ranks(p0.elapsed_time(p1), world, dev)
+    e0, e1 = e2e_run(1)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = job_tokens_per_s(wl.B, world, args.steps, e2e_ms)
     h2d = px[0].numel() * 2 + pids[0].numel() * 4 + pw[0].numel() * 4
-    d2h = py.numel() * 4
+    d2h = e2e_bufs[0]["py"].numel() * 4
 
     if rank != 0:
         return
@@ -464,7 +484,11 @@ def run_ours(args, wl, rank, world, local_rank):
                      "traffic": traffic},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "api": "moe_layer_host, one stream",
+                "pipelined": {"value": job_tokens_per_s(wl.B, world, args.steps, e2e_pipe_ms),
+                              "unit": "tokens/s",
+                              "how": "moe_layer_host on 2 streams taking alternate steps; one "
+                                     "step's copies and kernels overlap the other's"}},
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(wall0, wall1),
     }
