@@ -59,7 +59,8 @@ def q30():
     return Layer(workload.SHAPES["q30"])
 
 
-@pytest.mark.parametrize("B", [1, 32])
+# B=1, 2, 4 and 32 run moe_down with 1 x 8, 2 x 4, 4 x 2 and 8 x 1 outputs x units per lane
+@pytest.mark.parametrize("B", [1, 2, 4, 32])
 def test_layer_from_logits(q30, B):
     """moe_layer_routed == moe_layer fed moe_route's routing (bit for bit), and
     matches the oracle layer fed the oracle's routing."""
