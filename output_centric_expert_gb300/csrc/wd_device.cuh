@@ -30,12 +30,18 @@
 //    1 KB of one row contiguously. Weight loads bypass L1 allocation; reuse of
 //    a row by several tokens happens in L2, which the grid order makes likely
 //    (neuron/output block is the slow grid axis, tokens the fast one).
-//  * Latency is hidden by occupancy: both kernels are kept at <= 80 registers
-//    so that 3 CTAs (24 warps) fit on an SM. (Holding a second unit of codes in
-//    registers to prefetch it, or staging codes through a cp.async ring in
-//    shared memory, both measured slower on this part.) moe_gate_up warps loop
-//    over several routed slots of one token; moe_down warps own several
-//    outputs that share one read of the intermediate from shared memory.
+//  * Latency is hidden by occupancy. moe_gate_up stays at 80 registers, so 3
+//    CTAs (24 warps) fit on an SM; its warps loop over several routed slots of
+//    one token. moe_down warps own several outputs that share one read of the
+//    intermediate from shared memory. They use 80 registers with at most 4
+//    rows in flight per lane, and 128 registers (2 CTAs per SM) when a lane
+//    holds 8 rows' codes: 8 outputs, or fewer outputs with several units at
+//    once on small batches. (Holding a second unit of codes to prefetch it,
+//    staging codes through a cp.async or bulk-copy ring in shared memory, and
+//    refilling registers row by row all measured slower on this part.)
+//  * Row strides. The kernels are also compiled with the row length as a
+//    constant for the hidden and intermediate sizes of the target layers, so
+//    strides and offsets are load immediates (wd_gate_up_fixed.cu, wd_down.cu).
 #pragma once
 
 #include <cuda_bf16.h>

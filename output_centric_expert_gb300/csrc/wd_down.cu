@@ -23,8 +23,9 @@ struct DownUnit {
 };
 
 // UPL: units each lane requests at once. When the whole grid fits on the GPU
-// in one wave (small batches), a lane with one output has registers to keep
-// UPL of its (slot, block) units in flight instead of one HBM round trip each.
+// in one wave (small batches), a lane with OPW < 8 outputs has registers to
+// keep UPL = 8 / OPW of its (slot, block) units in flight instead of one HBM
+// round trip each.
 // KI: the row length I fixed at compile time (0: taken from the argument). With
 // it the row strides are constants the loads take as immediates, and the
 // (slot, block) advance divides by a constant.
