@@ -128,15 +128,44 @@ def test_q30_gate_up_kernel_alone(q30):
     _check_h(h.cpu().numpy().view(np.uint16), h_ref)
 
 
-def test_q235_sampled_tokens():
-    """Qwen-3-235B-A22B-shaped layer at B=64 (full size); the oracle checks 3 tokens."""
+def _sample(B, n):
+    """Up to n token indices spread over the batch, first and last included."""
+    return sorted(set(np.linspace(0, B - 1, min(n, B)).round().astype(int).tolist()))
+
+
+@pytest.mark.parametrize("B,routing", [(B, r) for r in ("uniform", "skewed") for B in (1, 2, 4, 8, 16, 32, 64)])
+def test_sweep_config_sampled_tokens(q30, B, routing):
+    """Every point of the Qwen-3-30B-A3B-shaped batch sweep, on the bench's first
+    batch of that config: up to 8 tokens against the oracle."""
+    x, ids, w = workload.tokens(q30.shape, B, routing=routing)
+    y, h = _run_layer(q30, x, ids, w)
+    sample = _sample(B, 8)
+    y_ref, h_ref, _ = oracle.moe_layer(q30.ref, x[sample], ids[sample], w[sample], return_h=True)
+    _check_y(y[sample], y_ref)
+    _check_h(h[sample], h_ref)
+
+
+Q235_BATCHES = (1, 16, 64)
+
+
+@pytest.fixture(scope="module")
+def q235():
     s = workload.SHAPES["q235"]
-    B = 64
-    x, ids, w = workload.tokens(s, B)
-    sample = [0, 31, 63]
-    layer = Layer(s, oracle_experts=np.unique(ids[sample]))
-    y, _ = _run_layer(layer, x, ids, w)
-    y_ref, _ = oracle.moe_layer(layer.ref, x[sample], ids[sample], w[sample])
+    need = set()
+    for B in Q235_BATCHES:
+        _, ids, _ = workload.tokens(s, B)
+        need |= set(ids[_sample(B, 3)].ravel().tolist())
+    return Layer(s, oracle_experts=sorted(need))
+
+
+@pytest.mark.parametrize("B", Q235_BATCHES)
+def test_q235_sampled_tokens(q235, B):
+    """Qwen-3-235B-A22B-shaped layer (full size, all 128 experts on the device) at
+    the configured batches; the oracle checks 3 tokens of each."""
+    x, ids, w = workload.tokens(q235.shape, B)
+    sample = _sample(B, 3)
+    y, _ = _run_layer(q235, x, ids, w)
+    y_ref, _ = oracle.moe_layer(q235.ref, x[sample], ids[sample], w[sample])
     _check_y(y[sample], y_ref)
     assert np.all(np.isfinite(y))
 
@@ -173,6 +202,7 @@ def _rand_layer_shape(H, I, E, k, seed=0):
     (544, 64, 3, 3, 2),       # top_k = E
     (256, 128, 8, 8, 4),      # tiny layer with k = E
     (96, 160, 5, 3, 128),     # H % 64 != 0 where 8 outputs per warp would leave outputs unwritten
+    (96, 160, 5, 3, 10),      # 2 slots per warp with top_k = 3: the second group has one slot
 ])
 def test_ragged_and_small_shapes(H, I, E, k, B):
     layer = _rand_layer_shape(H, I, E, k, seed=H + I)
