@@ -59,7 +59,7 @@ constexpr int kWarpsPerCta = 8;  // 8 warps per CTA, as the pages give for moe_g
 constexpr int kThreads = kWarpsPerCta * 32;
 constexpr int kSegBlocksPerLane = 2;               // gate/up: 32-element blocks per lane per unit
 constexpr int kSegBlocks = 32 * kSegBlocksPerLane;  // blocks of one row per unit (2048 elements)
-constexpr int kMinCtas = 8 * 152;                  // enough CTAs to fill 152 SMs several times
+constexpr int kMinCtasPerSm = 8;                    // CTAs per SM that fill the GPU several times
 
 constexpr int kRouteMaxE = 256;
 
@@ -77,6 +77,10 @@ void set_error(const char* what, cudaError_t e);
 void set_error_msg(const char* msg);
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Number of SMs of the current device (looked up once per device; 152 on a
+// GB300). Only the launch heuristics use it: grids stay correct for any value.
+int sm_count();
 
 constexpr size_t kMaxDynSmem = 227 * 1024;
 

@@ -143,15 +143,16 @@ __global__ void __launch_bounds__(kThreads, (OPW * UPL >= 8) ? 2 : 3)
 // Outputs per warp of moe_down beyond the single-wave small batches: 8 for
 // rows of at most 1024 elements (measured faster there from B=16 up: Q30
 // B=16 39.5 -> 31.1 us against 2 outputs per warp; slower for the 1536-element
-// rows of the 235B-shaped layer), else as many as keep at least kMinCtas CTAs.
+// rows of the 235B-shaped layer), else as many as keep at least kMinCtasPerSm
+// CTAs per SM.
 // A CTA covers 8 * OPW outputs, so OPW = 8 needs H % 64 == 0 (H % 32 == 0 is
 // enough for the others).
-int pick_opw(int B, int H, int I) {
+int pick_opw(int B, int H, int I, int sms) {
   if (H % (kWarpsPerCta * 8) == 0 && I <= 1024) return 8;
   const int opws[3] = {4, 2, 1};
   for (int v : opws) {
     const int64_t ctas = (int64_t)B * (H / (kWarpsPerCta * v));
-    if (ctas >= kMinCtas) return v;
+    if (ctas >= (int64_t)kMinCtasPerSm * sms) return v;
   }
   return 1;
 }
@@ -213,15 +214,16 @@ moe_status launch_down_kernels(const moe_shape* s, const moe_weights* w, const u
   // Fewer, fuller CTAs stage each token's intermediate fewer times and need
   // fewer round trips per lane than one-output warps (Q30 B=8: 32.6 -> 18.5 us).
   const int64_t ctas_opw1 = (int64_t)B * (s->H / kWarpsPerCta);
-  if (ctas_opw1 <= 2 * 152)
+  const int64_t wave = 2 * (int64_t)sm_count();
+  if (ctas_opw1 <= wave)
     return launch_down<1, 8>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
-  if (ctas_opw1 / 2 <= 2 * 152)
+  if (ctas_opw1 / 2 <= wave)
     return launch_down<2, 4>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
-  if (ctas_opw1 / 4 <= 2 * 152)
+  if (ctas_opw1 / 4 <= wave)
     return launch_down<4, 2>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
-  if (s->H % (kWarpsPerCta * 8) == 0 && ctas_opw1 / 8 <= 2 * 152)
+  if (s->H % (kWarpsPerCta * 8) == 0 && ctas_opw1 / 8 <= wave)
     return launch_down<8, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
-  switch (pick_opw(B, s->H, s->I)) {
+  switch (pick_opw(B, s->H, s->I, sm_count())) {
     case 8: return launch_down<8, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
     case 4: return launch_down<4, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
     case 2: return launch_down<2, 1>(s, w, h, ids, wts, B, y, err, st, dependent, logits);

@@ -11,19 +11,20 @@ namespace {
 // segment) units to stream one after the other (measured: Q30 B=2 19.5 ->
 // 18.1 us, B=4 29.7 -> 28.3, Q235 B=1 34.6 -> 33.0; 32 units per warp for the
 // DeepSeek-V3-shaped layer at B=1 was slower). Otherwise as many as keep at
-// least kMinCtas CTAs.
+// least kMinCtasPerSm CTAs per SM.
 int pick_spw(int B, int top_k, int I, int nseg) {
+  const int sms = sm_count();
   const int small[4] = {1, 2, 4, 8};
   for (int v : small) {
     if ((v > top_k && v > 1) || v * nseg > 8) break;
     const int64_t ctas = (int64_t)B * ((top_k + v - 1) / v) * (I / kWarpsPerCta);
-    if (ctas <= 3 * 152) return v;
+    if (ctas <= 3 * sms) return v;
   }
   const int spws[4] = {8, 4, 2, 1};
   for (int v : spws) {
     if (v > top_k) continue;
     const int64_t ctas = (int64_t)B * ((top_k + v - 1) / v) * (I / kWarpsPerCta);
-    if (ctas >= kMinCtas) return v;
+    if (ctas >= (int64_t)kMinCtasPerSm * sms) return v;
   }
   return 1;
 }
