@@ -129,3 +129,53 @@ def test_packer_per_expert_slices_equal_whole_pack():
     for a, b in zip((whole.gu_codes, whole.gu_scales, whole.d_codes, whole.d_scales),
                     (parts.gu_codes, parts.gu_scales, parts.d_codes, parts.d_scales)):
         assert np.array_equal(a, b)
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "warp_decode.h"
+
+/* every entry point, taken by address: the program links only if all exist */
+typedef void (*any_fn)(void);
+static const any_fn entry_points[] = {
+  (any_fn)moe_packed_bytes, (any_fn)moe_pack_weights, (any_fn)moe_gate_up, (any_fn)moe_down,
+  (any_fn)moe_layer, (any_fn)moe_layer_host, (any_fn)moe_route, (any_fn)moe_layer_routed,
+  (any_fn)moe_layer_noalloc, (any_fn)moe_status_string, (any_fn)moe_last_error,
+};
+
+int main(void) {
+  moe_shape s = {2048, 768, 128, 8};
+  size_t gu = moe_packed_bytes(&s, 0), ds = moe_packed_bytes(&s, 3);
+  moe_shape bad = {100, 768, 128, 8};  /* H % 32 != 0 */
+  moe_status rc = moe_gate_up(&bad, NULL, NULL, NULL, 1, NULL, NULL, NULL);
+  printf("%zu %zu %d %s %d\n", gu, ds, (int)rc, moe_status_string(rc),
+         (int)(sizeof entry_points / sizeof entry_points[0]));
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """The header compiles as C11 (gcc, no C++), a C program links against the
+    library with every entry point, and host-only calls behave as documented."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    lib = ops.lib()._name
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER),
+                    str(src), lib, f"-Wl,-rpath,{os.path.dirname(lib)}", "-o", str(exe)],
+                   check=True, capture_output=True, text=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    sh = ops.make_shape(2048, 768, 128, 8)
+    assert int(out[0]) == ops.moe_packed_bytes(sh, 0)
+    assert int(out[1]) == ops.moe_packed_bytes(sh, 3)
+    assert int(out[2]) == 2  # MOE_ERR_SHAPE, before any CUDA call
+    assert out[3:5] == ["unsupported", "shape"]
+    assert int(out[5]) == len(_declared_functions())
