@@ -474,6 +474,9 @@ def run_ours(args, wl, rank, world, local_rank):
                          f"({N_LAYERS * layers[0].nbytes / 1e9:.2f} GB) alternate per step, "
                          f"{N_BATCHES} token batches cycle",
                    "layer_gbs": layer_gbs, "layer_frac_of_peak": layer_gbs / peak,
+                   # the pages' one absolute figure for this layer and batch, measured on
+                   # B200 (context, not a target): 3.95 TB/s effective bandwidth at B=32
+                   "pages_b200_gbs_b32": 3950.0 if (wl.shape.H, wl.shape.I, wl.B) == (2048, 768, 32) else None,
                    "layer_bytes_per_step": sum(lay_bytes) / args.steps,
                    "gate_up_us": sum(gu_ms) / args.steps * 1e3,
                    "down_us": sum(dn_ms) / args.steps * 1e3,
