@@ -167,12 +167,15 @@ moe_status moe_route(const moe_shape* shape, const float* logits, int32_t B, int
                      float* wts, void* stream);
 
 /*
- * moe_layer_routed -- the layer from router logits, still two kernels: every
- * moe_gate_up and moe_down warp routes its token from `logits` itself (the
- * same choice as moe_route), so no ids/weights array has to exist between
- * router and layer. If ids_out and wts_out are both non-NULL, the routing is
- * also written there ([B][top_k], as moe_route). Same limits as moe_route;
- * other arguments as for moe_layer.
+ * moe_layer_routed -- the layer from router logits (the same choice as
+ * moe_route). Two ways, the same results bit for bit:
+ *  - ids_out and wts_out both non-NULL ([B][top_k], as moe_route): every token
+ *    is routed once into them by the router kernel, and the two layer kernels
+ *    read that routing. The faster way.
+ *  - both NULL: no ids/weights array exists at all. Every CTA of moe_gate_up
+ *    and moe_down routes its token from `logits` itself before it requests
+ *    weights, which costs about 25 % of the layer at B=32.
+ * Same limits as moe_route; other arguments as for moe_layer.
  */
 moe_status moe_layer_routed(const moe_shape* shape, const moe_weights* w, const uint16_t* x,
                             const float* logits, int32_t B, uint16_t* h_scratch, float* y,

@@ -65,11 +65,9 @@ constexpr int kRouteMaxE = 256;
 
 struct RouteArgs {
   const float* logits;  // [B][E], or nullptr: the ids/wts arrays are the routing
-  int32_t* ids_out;     // routing chosen by the kernel, written if non-null
-  float* w_out;
 };
 
-constexpr RouteArgs kNoRoute = {nullptr, nullptr, nullptr};
+constexpr RouteArgs kNoRoute = {nullptr};
 
 // ------------------------------------------------------ host helpers (shared) --
 // Defined with the C-ABI entry points; one error message per calling thread.
