@@ -172,9 +172,9 @@ moe_status moe_route(const moe_shape* shape, const float* logits, int32_t B, int
  *  - ids_out and wts_out both non-NULL ([B][top_k], as moe_route): every token
  *    is routed once into them by the router kernel, and the two layer kernels
  *    read that routing. The faster way.
- *  - both NULL: no ids/weights array exists at all. Every CTA of moe_gate_up
+ *  - both NULL: no ids/weights array exists at all. Every warp of moe_gate_up
  *    and moe_down routes its token from `logits` itself before it requests
- *    weights, which costs about 25 % of the layer at B=32.
+ *    weights, which costs about 30 % of the layer at B=32.
  * Same limits as moe_route; other arguments as for moe_layer.
  */
 moe_status moe_layer_routed(const moe_shape* shape, const moe_weights* w, const uint16_t* x,

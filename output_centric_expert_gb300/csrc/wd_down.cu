@@ -98,21 +98,19 @@ __global__ void __launch_bounds__(kThreads, (OPW * UPL >= 8) ? 2 : 3)
   // The ids, routing weights and down weights are inputs of the layer, not
   // produced by moe_gate_up: the first batch is requested before waiting for
   // the intermediate.
-  if (logits) {  // route the token here, from its logits (same result as gate_up):
-                 // warp 0 routes, the other warps read its choice
-    if (threadIdx.x < 32) {
-      int rid;
-      float rw;
-      warp_route(logits + (size_t)t * E, E, top_k, rid, rw);
-      if (lane < top_k) {
-        s_ids[lane] = rid;
-        s_w[lane] = rw;
-      }
-    }
-    __syncthreads();
+  if (logits) {  // route the token here, from its logits (same result as gate_up)
+    int rid;
+    float rw;
+    warp_route(logits + (size_t)t * E, E, top_k, rid, rw);
 #pragma unroll
-    for (int q = 0; q < UPL; ++q)
-      if (lane + 32 * q < units) load_unit(s_ids[jj[q]], bb[q], U[q]);
+    for (int q = 0; q < UPL; ++q) {
+      const int e = __shfl_sync(0xFFFFFFFFu, rid, jj[q] < top_k ? jj[q] : 0);
+      if (lane + 32 * q < units) load_unit(e, bb[q], U[q]);
+    }
+    if (threadIdx.x < top_k) {
+      s_ids[threadIdx.x] = rid;
+      s_w[threadIdx.x] = rw;
+    }
   } else {
 #pragma unroll
     for (int q = 0; q < UPL; ++q)

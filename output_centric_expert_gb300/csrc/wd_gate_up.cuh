@@ -51,18 +51,14 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   // lane s < nslots holds the expert id of slot s; -1 marks "no slot"
   int e_lane;
-  if (route.logits) {  // route the token here, from its logits: warp 0 routes, the
-                       // other warps read its choice (routing every warp cost 31 %
-                       // of the layer at Q30 B=32)
-    __shared__ int s_route[32];
-    if (threadIdx.x < 32) {
-      int rid;
-      float rw;
-      warp_route(route.logits + (size_t)t * E, E, top_k, rid, rw);
-      s_route[lane] = rid;
-    }
-    __syncthreads();
-    e_lane = (lane < nslots) ? s_route[j0 + lane] : -1;
+  if (route.logits) {  // route the token here, from its logits (every warp routes: a
+                       // barrier here, to route once per CTA, slowed the kernel for
+                       // the 235B-shaped layer even when no logits are given)
+    int rid;
+    float rw;
+    warp_route(route.logits + (size_t)t * E, E, top_k, rid, rw);
+    e_lane = __shfl_sync(0xFFFFFFFFu, rid, lane < nslots ? j0 + lane : 0);
+    if (lane >= nslots) e_lane = -1;
   } else {
     e_lane = (lane < nslots) ? __ldg(ids + (size_t)t * top_k + j0 + lane) : -1;
   }
