@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, (OPW * UPL >= 8) ? 2 : 3)
     }
   }
   wait_prerequisite();  // the intermediate h is complete from here on
-  const int sigma = stage_activations(h + (size_t)t * top_k * I, top_k, I, hs, red);
+  const int sigma = stage_activations<true>(h + (size_t)t * top_k * I, top_k, I, hs, red);
   const float unscale = exp2i(-sigma);
 
   if constexpr (OPW == 8 && UPL == 1) {
