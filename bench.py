@@ -9,7 +9,7 @@ headline point ("Better MoE model inference with warp decode", Key claims
 [§Hardware Efficiency]: 3.95 TB/s at B=32 on B200).
 
 L2 hygiene: two different layers' MXFP8 weights (2 x 623 MB, far above the
-126 MB L2) alternate step by step, and every step uses a different batch of
+129 MB L2) alternate step by step, and every step uses a different batch of
 tokens, so no step finds its weights in L2 (a real decode step also reads a
 different layer's weights each time).
 
