@@ -273,6 +273,36 @@ def oracle_baseline(wl, seconds: float, seed: int = 0):
     return tokens / el, f"{i} batches x {wl.B} tokens of {wl.name} (layer 0), {el:.1f} s"
 
 
+def oracle_baseline_all_cores(wl, seconds: float, seed: int = 0):
+    """The same oracle, unchanged, on every host core: each batch's tokens are
+    handed to a thread pool one token per task (the C oracle runs with the GIL
+    released). Returns tokens/s, the sample and the thread count."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    cores = os.cpu_count() or 1
+    batches = make_batches(wl, 4, seed)
+    need = np.unique(np.concatenate([b[1].ravel() for b in batches]))
+    ref = _oracle_layer(wl.shape, seed, 0, need)
+    # one call before any thread starts: the oracle fills its decode tables on
+    # first use, and thread creation orders that before every worker's reads
+    x, ids, w = batches[0]
+    oracle.moe_layer(ref, x[:1], ids[:1], w[:1])
+    tokens, i = 0, 0
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        t0 = time.perf_counter()
+        while True:
+            x, ids, w = batches[i % len(batches)]
+            list(ex.map(lambda t: oracle.moe_layer(ref, x[t:t + 1], ids[t:t + 1], w[t:t + 1]),
+                        range(wl.B)))
+            tokens += wl.B
+            i += 1
+            el = time.perf_counter() - t0
+            if el >= seconds or i >= 256:
+                break
+    return tokens / el, f"{i} batches x {wl.B} tokens of {wl.name} (layer 0), {el:.1f} s", cores
+
+
 def _oracle_layer(shape, seed, layer, experts):
     from concurrent.futures import ThreadPoolExecutor
 
@@ -456,10 +486,13 @@ def run_ours(args, wl, rank, world, local_rank):
 
     if rank != 0:
         return
-    cpu = None
+    cpu = cpu_all = None
     if not args.no_cpu_baseline:
         v, sample = oracle_baseline(wl, args.cpu_seconds)
         cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
+        v, sample, cores = oracle_baseline_all_cores(wl, args.cpu_seconds)
+        cpu_all = {"value": v, "unit": "tokens/s", "cores": cores,
+                   "kind": "oracle, one token per thread", "sample": sample}
     traffic = ncu_traffic("moe_gate_up", wl.name)
     gu_launch_bytes = sum(gu_bytes) / args.steps
     out = {
@@ -486,6 +519,7 @@ def run_ours(args, wl, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": gu_launch_bytes,
                      "traffic": traffic},
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "api": "moe_layer_host, one stream",
                 "pipelined": {"value": job_tokens_per_s(wl.B, world, args.steps, e2e_pipe_ms),
