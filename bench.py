@@ -94,6 +94,7 @@ def measured_peaks():
 
 KERNEL_SOURCES = {
     "moe_gate_up": ["wd_device.cuh", "wd_gate_up.cuh", "wd_gate_up.cu", "wd_gate_up_fixed.cu"],
+    "moe_gate_up_grouped": ["wd_device.cuh", "wd_gate_up_grouped.cu"],
     "moe_down": ["wd_device.cuh", "wd_down.cu"],
 }
 
@@ -415,13 +416,17 @@ def run_ours(args, wl, rank, world, local_rank):
         raise RuntimeError("device error flag set: an expert id was out of range")
 
     # ---- per-kernel durations (same steps, an event between the kernels) --
+    # the gate/up kernel the layer itself runs at this shape and batch
+    gu_kernel = "moe_gate_up_grouped" if ops.layer_gate_up_kernel(layers[0].shape, wl.B) == "grouped" \
+        else "moe_gate_up"
+    gate_up_fn = getattr(ops, gu_kernel)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     barrier()
     for i in range(args.steps):
         b = i % N_BATCHES
         L = layers[i % N_LAYERS]
         evs[i][0].record(stream)
-        ops.moe_gate_up(L, dx[b], dids[b], h, err, stream)
+        gate_up_fn(L, dx[b], dids[b], h, err, stream)
         evs[i][1].record(stream)
         ops.moe_down(L, h, dids[b], dw[b], y, err, stream)
         evs[i][2].record(stream)
@@ -493,7 +498,7 @@ def run_ours(args, wl, rank, world, local_rank):
         v, sample, cores = oracle_baseline_all_cores(wl, args.cpu_seconds)
         cpu_all = {"value": v, "unit": "tokens/s", "cores": cores,
                    "kind": "oracle, one token per thread", "sample": sample}
-    traffic = ncu_traffic("moe_gate_up", wl.name)
+    traffic = ncu_traffic(gu_kernel, wl.name)
     gu_launch_bytes = sum(gu_bytes) / args.steps
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -514,7 +519,7 @@ def run_ours(args, wl, rank, world, local_rank):
                    "gate_up_us": sum(gu_ms) / args.steps * 1e3,
                    "down_us": sum(dn_ms) / args.steps * 1e3,
                    "down_gbs": dn_gbs},
-        "roofline": {"bound": "hbm", "kernel": "moe_gate_up", "achieved": gu_gbs, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": gu_kernel, "achieved": gu_gbs, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": gu_gbs / peak,
                      "algorithmic_bytes_per_launch": gu_launch_bytes,
                      "traffic": traffic},
@@ -607,7 +612,9 @@ def run_sweep(names, steps: int):
         lay_bytes = float(np.mean([layer_bytes(s, b[1]) for b in batches]))
         uniq = float(np.mean([len(np.unique(b[1])) for b in batches]))
         print(json.dumps({"workload": name, "H": s.H, "I": s.I, "E": s.E, "top_k": s.top_k,
-                          "B": wl.B, "routing": wl.routing, "us_per_layer": round(us, 2),
+                          "B": wl.B, "routing": wl.routing,
+                          "gate_up_kernel": ops.layer_gate_up_kernel(layers[0].shape, wl.B),
+                          "us_per_layer": round(us, 2),
                           "tokens_per_s": round(wl.B / us * 1e6), "unique_experts": uniq,
                           "layer_bytes": lay_bytes, "layer_gbs": round(lay_bytes / us / 1e3, 1),
                           "frac_of_measured_peak": round(lay_bytes / us / 1e3 / peak, 4),

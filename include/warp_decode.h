@@ -116,6 +116,28 @@ moe_status moe_gate_up(const moe_shape* shape, const moe_weights* w, const uint1
                        void* stream);
 
 /*
+ * moe_gate_up_grouped -- moe_gate_up computed by its expert-grouped kernel:
+ * one warp per (expert, 8 neurons) serves every (token, slot) pair routed to
+ * that expert, decoding each weight once and multiplying on the tensor cores
+ * (mma.sync m16n8k16, f16 operands, FP32 accumulation; rows are the gate and
+ * up rows of the 8 neurons, columns 8 of the routed pairs). Each warp still
+ * writes its own outputs h[t,j,n] once, with no buffer, gather or scatter
+ * ("Better MoE model inference with warp decode", [§How the two kernels
+ * work]; the routed experts of [§Reorganized parallelism]). Arguments and
+ * result as for moe_gate_up; the sums differ from moe_gate_up's only in
+ * FP32 rounding order; a pair's result does not depend on the other pairs
+ * of the batch. Returns MOE_ERR_UNSUPPORTED, launching nothing, unless
+ * H % 256 == 0, I % 64 == 0 and gu_scales is 4-byte aligned.
+ * moe_layer and the other layer entry points use this kernel by themselves
+ * when B * top_k >= 3 * E and the shape allows it (measured faster there on
+ * GB300: each weight is decoded once instead of once per pair); below that,
+ * and when routing from logits without ids_out, they use moe_gate_up's kernel.
+ */
+moe_status moe_gate_up_grouped(const moe_shape* shape, const moe_weights* w,
+                               const uint16_t* x, const int32_t* ids, int32_t B, uint16_t* h,
+                               int32_t* err_flag, void* stream);
+
+/*
  * moe_down -- second kernel ("moe_down_3d_batched" on the pages).
  *   h    [B][top_k][I] BF16 intermediate from moe_gate_up (device)
  *   ids  [B][top_k]    int32 expert ids (device)

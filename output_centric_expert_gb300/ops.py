@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
         L.moe_pack_weights.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_gate_up.restype = ctypes.c_int
         L.moe_gate_up.argtypes = [sp, wp, vp, vp, i32, vp, vp, vp]
+        L.moe_gate_up_grouped.restype = ctypes.c_int
+        L.moe_gate_up_grouped.argtypes = [sp, wp, vp, vp, i32, vp, vp, vp]
         L.moe_down.restype = ctypes.c_int
         L.moe_down.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp]
         L.moe_layer.restype = ctypes.c_int
@@ -178,6 +180,30 @@ def moe_gate_up(weights: DeviceWeights, x: torch.Tensor, ids: torch.Tensor, h: t
     return h
 
 
+def moe_gate_up_grouped(weights: DeviceWeights, x: torch.Tensor, ids: torch.Tensor,
+                        h: torch.Tensor, err_flag: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """moe_gate_up by the expert-grouped kernel (tensor-core MMAs over the pairs
+    routed to each expert); same result up to FP32 rounding order."""
+    B = x.shape[0]
+    _check("moe_gate_up_grouped", lib().moe_gate_up_grouped(
+        ctypes.byref(weights.shape), ctypes.byref(weights.struct), _ptr(x, _BF16, "x"),
+        _ptr(ids, (torch.int32,), "ids"), B, _ptr(h, _BF16, "h"),
+        _ptr(err_flag, (torch.int32,), "err_flag"), _stream(stream)))
+    return h
+
+
+def layer_gate_up_kernel(shape: MoeShape, B: int) -> str:
+    """The moe_gate_up kernel the layer entry points run for `shape` at batch B,
+    by the library's rule: "grouped" (moe_gate_up_grouped's) once
+    B * top_k >= 3 * E when that kernel takes the shape (H % 256 == 0,
+    I % 64 == 0), else "per_token" (moe_gate_up's). Scales are assumed 4-byte
+    aligned, as DeviceWeights allocates them."""
+    if (B * shape.top_k >= 3 * shape.E and shape.H % 256 == 0 and shape.I % 64 == 0):
+        return "grouped"
+    return "per_token"
+
+
 def moe_down(weights: DeviceWeights, h: torch.Tensor, ids: torch.Tensor, wts: torch.Tensor,
              y: torch.Tensor, err_flag: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """y[B,H] (fp32) = sum_j wts[:,j] * (h[:,j] Wd[ids[:,j]]^T)."""
@@ -268,6 +294,7 @@ def moe_layer_host(weights: DeviceWeights, x_host: torch.Tensor, ids_host: torch
 
 def exported_symbols() -> list[str]:
     """The entry points include/warp_decode.h declares."""
-    return ["moe_packed_bytes", "moe_pack_weights", "moe_gate_up", "moe_down", "moe_layer",
+    return ["moe_packed_bytes", "moe_pack_weights", "moe_gate_up", "moe_gate_up_grouped",
+            "moe_down", "moe_layer",
             "moe_layer_host", "moe_layer_noalloc", "moe_route", "moe_layer_routed",
             "moe_status_string", "moe_last_error"]

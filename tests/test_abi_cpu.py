@@ -139,7 +139,8 @@ C_CLIENT = r"""
 /* every entry point, taken by address: the program links only if all exist */
 typedef void (*any_fn)(void);
 static const any_fn entry_points[] = {
-  (any_fn)moe_packed_bytes, (any_fn)moe_pack_weights, (any_fn)moe_gate_up, (any_fn)moe_down,
+  (any_fn)moe_packed_bytes, (any_fn)moe_pack_weights, (any_fn)moe_gate_up,
+  (any_fn)moe_gate_up_grouped, (any_fn)moe_down,
   (any_fn)moe_layer, (any_fn)moe_layer_host, (any_fn)moe_route, (any_fn)moe_layer_routed,
   (any_fn)moe_layer_noalloc, (any_fn)moe_status_string, (any_fn)moe_last_error,
 };
@@ -179,3 +180,15 @@ def test_header_is_plain_c_and_links(tmp_path):
     assert int(out[2]) == 2  # MOE_ERR_SHAPE, before any CUDA call
     assert out[3:5] == ["unsupported", "shape"]
     assert int(out[5]) == len(_declared_functions())
+
+
+def test_layer_gate_up_kernel_rule():
+    """The binding's statement of the layer's kernel choice: the grouped kernel
+    from B*top_k >= 3E when it takes the shape (the GPU test
+    test_layer_uses_the_grouped_kernel_from_3e_pairs checks the library)."""
+    q30 = ops.make_shape(2048, 768, 128, 8)
+    assert ops.layer_gate_up_kernel(q30, 47) == "per_token"
+    assert ops.layer_gate_up_kernel(q30, 48) == "grouped"
+    assert ops.layer_gate_up_kernel(ops.make_shape(2080, 768, 128, 8), 64) == "per_token"
+    assert ops.layer_gate_up_kernel(ops.make_shape(2048, 96, 128, 8), 64) == "per_token"
+    assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 12) == "grouped"

@@ -262,18 +262,50 @@ def test_invalid_ids_flagged_and_skipped(tiny):
     _check_h(h, h_ref)
 
 
+@pytest.mark.parametrize("form", ["per_token", "grouped"])
 @pytest.mark.parametrize("which,B,routing", [("q30", 32, "uniform"), ("q30", 64, "skewed"), ("tiny", 16, "uniform")])
-def test_batch_equals_tokens_one_at_a_time(request, which, B, routing):
-    """A large batch runs with several slots per gate_up warp and several outputs
-    per down warp; a single token with one of each. Every (token, neuron) and
-    (token, output) sum is formed in the same order, so results must be identical."""
+def test_batch_equals_tokens_one_at_a_time(request, form, which, B, routing):
+    """A token's results do not depend on the rest of the batch, for each
+    moe_gate_up kernel. The per-token kernel runs a large batch with several
+    slots per warp and several outputs per down warp, a single token with one
+    of each, and forms every sum in the same order; the grouped kernel gives
+    each pair its own MMA column. Either way results must be identical. (The
+    layer entry points switch from the per-token to the grouped kernel at
+    B*top_k >= 3E; across that switch results agree to FP32 rounding only.)"""
     layer = request.getfixturevalue(which)
+    gate_up = ops.moe_gate_up if form == "per_token" else ops.moe_gate_up_grouped
     x, ids, w = workload.tokens(layer.shape, B, routing=routing, batch=500 + B)
-    y, h = _run_layer(layer, x, ids, w)
+
+    def run(xs, ids_, w_):
+        n = xs.shape[0]
+        h = torch.empty((n, layer.shape.top_k, layer.shape.I), dtype=torch.int16, device="cuda")
+        y = torch.empty((n, layer.shape.H), dtype=torch.float32, device="cuda")
+        idd = _dev(ids_)
+        gate_up(layer.dev, _dev(xs.view(np.int16)), idd, h)
+        ops.moe_down(layer.dev, h, idd, _dev(w_), y)
+        torch.cuda.synchronize()
+        return y.cpu().numpy(), h.cpu().numpy().view(np.uint16)
+
+    y, h = run(x, ids, w)
     for t in range(B):
-        y1, h1 = _run_layer(layer, x[t:t + 1], ids[t:t + 1], w[t:t + 1])
+        y1, h1 = run(x[t:t + 1], ids[t:t + 1], w[t:t + 1])
         assert np.array_equal(h1[0], h[t]), t
         assert np.array_equal(y1[0], y[t]), t
+
+
+def test_layer_uses_the_grouped_kernel_from_3e_pairs(q30):
+    """moe_layer's intermediate equals moe_gate_up's below B*top_k = 3E and
+    moe_gate_up_grouped's from there on (Qwen-3-30B-A3B shape: 48 tokens)."""
+    for B in (47, 48):
+        x, ids, w = workload.tokens(q30.shape, B, batch=700 + B)
+        _, h = _run_layer(q30, x, ids, w)
+        hp = torch.empty((B, 8, q30.shape.I), dtype=torch.int16, device="cuda")
+        hg = torch.empty_like(hp)
+        ops.moe_gate_up(q30.dev, _dev(x.view(np.int16)), _dev(ids), hp)
+        ops.moe_gate_up_grouped(q30.dev, _dev(x.view(np.int16)), _dev(ids), hg)
+        torch.cuda.synchronize()
+        want = (hg if B * 8 >= 3 * 128 else hp).cpu().numpy().view(np.uint16)
+        assert np.array_equal(h, want), B
 
 
 def test_invalid_ids_in_a_large_batch(tiny):
