@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work the oracle baseline sample aims at")
+    ap.add_argument("--gate-up-forms", action="store_true",
+                    help="with --sweep: also time moe_gate_up and moe_gate_up_grouped alone "
+                         "(CUDA graph, same rotation) for every workload")
     ap.add_argument("--sweep", nargs="*", default=None,
                     help="instead of the single contract line, print one line per workload "
                          "(default: the batch sweep of the pages' metric), timing CUDA-graph "
@@ -542,7 +545,7 @@ SWEEP_DEFAULT = ([f"q30_{r}_b{b}" for r in ("uniform", "skewed") for b in (1, 2,
 SWEEP_VARIANTS = ["dsv3_b1", "dsv3_b16", "dsv3_b64", "mixtral_b1", "mixtral_b16", "mixtral_b64"]
 
 
-def run_sweep(names, steps: int):
+def run_sweep(names, steps: int, gate_up_forms: bool = False):
     """Per workload: the layer (moe_layer, both kernels) captured in a CUDA graph
     over a rotation of 2 layers x 8 token batches, replayed; CUDA-event time per
     step. Launch overhead of the host is outside the measurement, as in a
@@ -611,6 +614,27 @@ def run_sweep(names, steps: int):
         warm_us = e0.elapsed_time(e1) * 1e3 / (reps * rot)
         lay_bytes = float(np.mean([layer_bytes(s, b[1]) for b in batches]))
         uniq = float(np.mean([len(np.unique(b[1])) for b in batches]))
+        forms = {}
+        if gate_up_forms:
+            # each gate/up kernel alone over the same rotation; GB/s of its own bytes
+            gu_b = float(np.mean([gate_up_bytes(s, b[1]) for b in batches]))
+            for form, fn in (("per_token", ops.moe_gate_up), ("grouped", ops.moe_gate_up_grouped)):
+                if form == "grouped" and not (s.H % 256 == 0 and s.I % 64 == 0):
+                    continue
+                gf = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gf):
+                    for i in range(rot):
+                        fn(layers[i % N_LAYERS], dx[i % N_BATCHES], dids[i % N_BATCHES], h)
+                for _ in range(2):
+                    gf.replay()
+                torch.cuda.synchronize(dev)
+                e0.record()
+                for _ in range(reps):
+                    gf.replay()
+                e1.record()
+                torch.cuda.synchronize(dev)
+                f_us = e0.elapsed_time(e1) * 1e3 / (reps * rot)
+                forms[form] = {"us": round(f_us, 2), "gbs": round(gu_b / f_us / 1e3, 1)}
         print(json.dumps({"workload": name, "H": s.H, "I": s.I, "E": s.E, "top_k": s.top_k,
                           "B": wl.B, "routing": wl.routing,
                           "gate_up_kernel": ops.layer_gate_up_kernel(layers[0].shape, wl.B),
@@ -620,14 +644,15 @@ def run_sweep(names, steps: int):
                           "frac_of_measured_peak": round(lay_bytes / us / 1e3 / peak, 4),
                           "timing": "CUDA graph of 16 steps (2 layers x 8 batches), replayed",
                           "warm_l2_us_per_layer": round(warm_us, 2),
-                          "warm_l2_bytes_per_layer": layer_bytes(s, batches[0][1])}),
+                          "warm_l2_bytes_per_layer": layer_bytes(s, batches[0][1]),
+                          **({"gate_up_alone": forms} if gate_up_forms else {})}),
               flush=True)
 
 
 def main():
     args = parse()
     if args.sweep is not None:
-        run_sweep(args.sweep or SWEEP_DEFAULT, args.steps)
+        run_sweep(args.sweep or SWEEP_DEFAULT, args.steps, args.gate_up_forms)
         return
     from output_centric_expert_gb300 import workload
     wl = workload.WORKLOADS[args.workload]

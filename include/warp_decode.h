@@ -127,11 +127,13 @@ moe_status moe_gate_up(const moe_shape* shape, const moe_weights* w, const uint1
  * result as for moe_gate_up; the sums differ from moe_gate_up's only in
  * FP32 rounding order; a pair's result does not depend on the other pairs
  * of the batch. Returns MOE_ERR_UNSUPPORTED, launching nothing, unless
- * H % 256 == 0, I % 64 == 0 and gu_scales is 4-byte aligned.
+ * H % 256 == 0, I % 64 == 0 and gu_scales is 8-byte aligned.
  * moe_layer and the other layer entry points use this kernel by themselves
- * when B * top_k >= 3 * E and the shape allows it (measured faster there on
- * GB300: each weight is decoded once instead of once per pair); below that,
- * and when routing from logits without ids_out, they use moe_gate_up's kernel.
+ * when 2 * B * top_k >= 5 * E and the shape allows it (measured faster there
+ * on GB300: each weight is decoded once instead of once per pair); below
+ * that, and when routing from logits without ids_out, they use moe_gate_up's
+ * kernel. The two kernels agree to FP32 rounding order, so a token's result
+ * can change in its last bits when the batch crosses that size.
  */
 moe_status moe_gate_up_grouped(const moe_shape* shape, const moe_weights* w,
                                const uint16_t* x, const int32_t* ids, int32_t B, uint16_t* h,

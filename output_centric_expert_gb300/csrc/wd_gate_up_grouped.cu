@@ -23,11 +23,13 @@
 // 32-element MXFP8 block the two MMAs sum the exact f16 x E4M3 products in
 // FP32 (the tensor core's own order), the block sum is multiplied by the
 // block's E8M0 scale and added to an FP32 accumulator. The k axis inside a
-// block is permuted identically for both operands (lane q of a quad takes
-// elements 8q..8q+7 of the block), which leaves the sum unchanged and lets
-// every lane load 8 contiguous codes. A column's result depends only on its
-// own pair, never on the other columns, so a token's intermediate does not
-// depend on the rest of the batch.
+// block is permuted identically for both operands: a quad of lanes loads 64
+// contiguous codes (two blocks, 16 codes per lane), the lanes q and q^2 swap
+// their upper 8 codes, and then lane q holds 8 codes of each block, at
+// element offset 16(q&1) + 8(q>>1) of the even block and 16(q&1) +
+// 8(1-(q>>1)) of the odd one; its activation reads use the same offsets. A
+// column's result depends only on its own pair, never on the other columns,
+// so a token's intermediate does not depend on the rest of the batch.
 //
 // Work. One CTA per (expert, 64-neuron tile); the CTA ranks the pairs routed
 // to its expert in pair order (CTAs of experts without pairs exit at once)
@@ -35,11 +37,14 @@
 // f16 x 2^sigma copy of the BF16 row as the per-token kernel (sigma per
 // token). Codes stream through registers, double-buffered 8 blocks deep.
 //
-// Measured on GB300 (Qwen-3-30B-A3B-shaped layer): faster than the per-token
-// kernel from about 48 tokens under uniform routing and at 32 tokens under
-// skewed routing; its loads (8 codes per lane, one 32-byte sector of each of
-// 8 rows per warp load) keep the L1 data pipe the busiest unit, so below
-// that the per-token kernel is used.
+// Loads. A warp load reads 64 contiguous bytes of each of 8 rows. With 8
+// bytes per lane (32 bytes per row) the L1 data pipe was the busiest unit
+// (about 60 % of peak against 47 % for DRAM, ncu, Qwen-3-30B-A3B shape at 32
+// tokens); 16 bytes per lane and the swap cut the kernel's time there from
+// 95.5 to 83.7 us with bit-identical results. Measured on GB300 it is faster
+// than the per-token kernel from about 36 tokens (Qwen-3-30B-A3B shape) or
+// 17 tokens (Qwen-3-235B-A22B shape) under uniform routing, and at 32 tokens
+// under skewed routing.
 #include "wd_device.cuh"
 
 namespace wd {
@@ -64,26 +69,27 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
         "f"(c[2]), "f"(c[3]));
 }
 
-// 8 codes (a lane's quarter of a 32-element block), not allocated in L1.
-__device__ __forceinline__ uint2 ld_codes8(const uint8_t* p) {
+// 16 codes (half of one of two adjacent 32-element blocks), not allocated in L1.
+__device__ __forceinline__ uint4 ld_codes16(const uint8_t* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+// The E8M0 scales of 8 consecutive blocks of one row.
+__device__ __forceinline__ uint2 ld_scales8(const uint8_t* p) {
   uint2 r;
   asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
   return r;
 }
 
-// The E8M0 scales of 4 consecutive blocks of one row.
-__device__ __forceinline__ uint32_t ld_scales4(const uint8_t* p) {
-  uint32_t r;
-  asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
-  return r;
-}
-
-// UNR: 32-element blocks per loop step (a multiple of 4: one 32-bit load of
-// scales per row per 4 blocks). NCH: column tiles of 8 pairs held at once.
+// UNR: 32-element blocks per loop step (a multiple of 8: one 64-bit load of
+// scales per row per 8 blocks). NCH: column tiles of 8 pairs held at once.
 template <int UNR>
 struct GrpBuf {
-  uint2 g[UNR], u[UNR];               // this lane's 8 codes of each block, gate and up row
-  uint32_t sg[UNR / 4], su[UNR / 4];  // scales, 4 blocks per word
+  uint4 g[UNR / 2], u[UNR / 2];    // this lane's 16 codes of each block pair, gate and up
+  uint2 sg[UNR / 8], su[UNR / 8];  // scales, 8 blocks per pair of words
 };
 
 template <int UNR, int NCH>
@@ -93,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                                const uint16_t* __restrict__ x, const int32_t* __restrict__ ids,
                                uint16_t* __restrict__ h, int32_t* __restrict__ err, int H, int I,
                                int E, int top_k, int B) {
-  static_assert(UNR % 4 == 0, "UNR: multiple of 4");
+  static_assert(UNR % 8 == 0, "UNR: multiple of 8");
   constexpr int kT = NCH * kGrpCols;  // pairs staged per pass
   extern __shared__ uint4 xs4[];      // [kT] rows of grp_row_bytes(H)
   __shared__ int s_pair[kT];          // pair index t*top_k + j of each staged column
@@ -127,25 +133,29 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
 
-  const uint8_t* grow = gu_codes + ((size_t)e * I + n) * 2 * H + q * 8;  // gate row, lane's 8 B
+  const uint8_t* grow = gu_codes + ((size_t)e * I + n) * 2 * H + q * 16;  // gate row, lane's 16 B
   const uint8_t* urow = grow + H;
   const uint8_t* gsc = gu_scales + ((size_t)e * I + n) * 2 * nblk;
   const uint8_t* usc = gsc + nblk;
-  const uint8_t* xl = xs + g * RS + q * 16;  // column g of tile 0, lane's 16 B of a block
+  const uint8_t* xl = xs + g * RS;  // column g of tile 0
 
   auto load = [&](int it, GrpBuf<UNR>& U) {
     const int b0 = it * UNR;
 #pragma unroll
-    for (int i = 0; i < UNR; ++i) {
-      U.g[i] = ld_codes8(grow + (size_t)(b0 + i) * 32);
-      U.u[i] = ld_codes8(urow + (size_t)(b0 + i) * 32);
+    for (int i = 0; i < UNR / 2; ++i) {
+      U.g[i] = ld_codes16(grow + (size_t)(b0 + 2 * i) * 32);
+      U.u[i] = ld_codes16(urow + (size_t)(b0 + 2 * i) * 32);
     }
 #pragma unroll
-    for (int i = 0; i < UNR / 4; ++i) {
-      U.sg[i] = ld_scales4(gsc + b0 + 4 * i);
-      U.su[i] = ld_scales4(usc + b0 + 4 * i);
+    for (int i = 0; i < UNR / 8; ++i) {
+      U.sg[i] = ld_scales8(gsc + b0 + 8 * i);
+      U.su[i] = ld_scales8(usc + b0 + 8 * i);
     }
   };
+  // element offset of this lane's 8 codes in an even and an odd block
+  const int off_even = 16 * (q & 1) + 8 * (q >> 1);
+  const int off_odd = 16 * (q & 1) + 8 * (1 - (q >> 1));
+  const bool low = q < 2;
 
   for (int lo = 0;; lo += kT) {
     // Rank the pairs routed to expert e in pair order; keep ranks [lo, lo+kT).
@@ -195,28 +205,43 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     auto compute = [&](int it, const GrpBuf<UNR>& U) {
 #pragma unroll
-      for (int i = 0; i < UNR; ++i) {
-        const int b = it * UNR + i;
-        // A fragments of the block's two k16 steps: {gate, up} x {k lo, k hi}
-        uint32_t a0[4], a1[4];
-        e4m3x4_to_f16x4(U.g[i].x, a0[0], a0[2]);
-        e4m3x4_to_f16x4(U.u[i].x, a0[1], a0[3]);
-        e4m3x4_to_f16x4(U.g[i].y, a1[0], a1[2]);
-        e4m3x4_to_f16x4(U.u[i].y, a1[1], a1[3]);
-        const float sg = e8m0_to_f32((U.sg[i / 4] >> (8 * (i % 4))) & 0xFFu);
-        const float su = e8m0_to_f32((U.su[i / 4] >> (8 * (i % 4))) & 0xFFu);
+      for (int i2 = 0; i2 < UNR / 2; ++i2) {
+        // swap upper halves with lane q^2: each lane then holds 8 codes of both blocks
+        const uint32_t rg2 = __shfl_xor_sync(0xFFFFFFFFu, U.g[i2].z, 2);
+        const uint32_t rg3 = __shfl_xor_sync(0xFFFFFFFFu, U.g[i2].w, 2);
+        const uint32_t ru2 = __shfl_xor_sync(0xFFFFFFFFu, U.u[i2].z, 2);
+        const uint32_t ru3 = __shfl_xor_sync(0xFFFFFFFFu, U.u[i2].w, 2);
+        const uint2 cgb[2] = {low ? make_uint2(U.g[i2].x, U.g[i2].y) : make_uint2(rg2, rg3),
+                              low ? make_uint2(rg2, rg3) : make_uint2(U.g[i2].x, U.g[i2].y)};
+        const uint2 cub[2] = {low ? make_uint2(U.u[i2].x, U.u[i2].y) : make_uint2(ru2, ru3),
+                              low ? make_uint2(ru2, ru3) : make_uint2(U.u[i2].x, U.u[i2].y)};
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          if (c < nch) {
-            const uint4 xv =
-                *reinterpret_cast<const uint4*>(xl + (size_t)c * kGrpCols * RS + b * 64);
-            float d[4];
-            mma_16816(d, a0, xv.x, xv.y, zero);
-            mma_16816(d, a1, xv.z, xv.w, d);
-            accg[c][0] = fmaf(d[0], sg, accg[c][0]);
-            accg[c][1] = fmaf(d[1], sg, accg[c][1]);
-            accu[c][0] = fmaf(d[2], su, accu[c][0]);
-            accu[c][1] = fmaf(d[3], su, accu[c][1]);
+        for (int hb = 0; hb < 2; ++hb) {
+          const int i = 2 * i2 + hb;
+          const int b = it * UNR + i;
+          uint32_t a0[4], a1[4];
+          e4m3x4_to_f16x4(cgb[hb].x, a0[0], a0[2]);
+          e4m3x4_to_f16x4(cub[hb].x, a0[1], a0[3]);
+          e4m3x4_to_f16x4(cgb[hb].y, a1[0], a1[2]);
+          e4m3x4_to_f16x4(cub[hb].y, a1[1], a1[3]);
+          const uint32_t swd = (i % 8) < 4 ? U.sg[i / 8].x : U.sg[i / 8].y;
+          const uint32_t uwd = (i % 8) < 4 ? U.su[i / 8].x : U.su[i / 8].y;
+          const float sg = e8m0_to_f32((swd >> (8 * (i % 4))) & 0xFFu);
+          const float su = e8m0_to_f32((uwd >> (8 * (i % 4))) & 0xFFu);
+          const int off = hb ? off_odd : off_even;
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            if (c < nch) {
+              const uint4 xv = *reinterpret_cast<const uint4*>(
+                  xl + (size_t)c * kGrpCols * RS + b * 64 + 2 * off);
+              float d[4];
+              mma_16816(d, a0, xv.x, xv.y, zero);
+              mma_16816(d, a1, xv.z, xv.w, d);
+              accg[c][0] = fmaf(d[0], sg, accg[c][0]);
+              accg[c][1] = fmaf(d[1], sg, accg[c][1]);
+              accu[c][0] = fmaf(d[2], su, accu[c][0]);
+              accu[c][1] = fmaf(d[3], su, accu[c][1]);
+            }
           }
         }
       }
@@ -269,7 +294,7 @@ constexpr int kGrpUnroll = 8;
 }  // namespace
 
 bool gate_up_grouped_supported(const moe_shape* s, const moe_weights* w) {
-  return s->H % (32 * kGrpUnroll) == 0 && s->I % kGrpNeurons == 0 && aligned(w->gu_scales, 4) &&
+  return s->H % (32 * kGrpUnroll) == 0 && s->I % kGrpNeurons == 0 && aligned(w->gu_scales, 8) &&
          (size_t)kGrpCols * grp_row_bytes(s->H) <= kMaxDynSmem &&
          (int64_t)s->E * (s->I / kGrpNeurons) <= 0x7FFFFFFF;
 }

@@ -196,10 +196,10 @@ def moe_gate_up_grouped(weights: DeviceWeights, x: torch.Tensor, ids: torch.Tens
 def layer_gate_up_kernel(shape: MoeShape, B: int) -> str:
     """The moe_gate_up kernel the layer entry points run for `shape` at batch B,
     by the library's rule: "grouped" (moe_gate_up_grouped's) once
-    B * top_k >= 3 * E when that kernel takes the shape (H % 256 == 0,
-    I % 64 == 0), else "per_token" (moe_gate_up's). Scales are assumed 4-byte
+    2 * B * top_k >= 5 * E when that kernel takes the shape (H % 256 == 0,
+    I % 64 == 0), else "per_token" (moe_gate_up's). Scales are assumed 8-byte
     aligned, as DeviceWeights allocates them."""
-    if (B * shape.top_k >= 3 * shape.E and shape.H % 256 == 0 and shape.I % 64 == 0):
+    if (2 * B * shape.top_k >= 5 * shape.E and shape.H % 256 == 0 and shape.I % 64 == 0):
         return "grouped"
     return "per_token"
 

@@ -184,11 +184,12 @@ def test_header_is_plain_c_and_links(tmp_path):
 
 def test_layer_gate_up_kernel_rule():
     """The binding's statement of the layer's kernel choice: the grouped kernel
-    from B*top_k >= 3E when it takes the shape (the GPU test
-    test_layer_uses_the_grouped_kernel_from_3e_pairs checks the library)."""
+    from 2*B*top_k >= 5E when it takes the shape (the GPU test
+    test_layer_uses_the_grouped_kernel_from_2_5e_pairs checks the library)."""
     q30 = ops.make_shape(2048, 768, 128, 8)
-    assert ops.layer_gate_up_kernel(q30, 47) == "per_token"
-    assert ops.layer_gate_up_kernel(q30, 48) == "grouped"
+    assert ops.layer_gate_up_kernel(q30, 39) == "per_token"
+    assert ops.layer_gate_up_kernel(q30, 40) == "grouped"
     assert ops.layer_gate_up_kernel(ops.make_shape(2080, 768, 128, 8), 64) == "per_token"
     assert ops.layer_gate_up_kernel(ops.make_shape(2048, 96, 128, 8), 64) == "per_token"
-    assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 12) == "grouped"
+    assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 9) == "per_token"
+    assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 10) == "grouped"
