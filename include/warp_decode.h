@@ -152,10 +152,12 @@ moe_status moe_down(const moe_shape* shape, const moe_weights* w, const uint16_t
                     int32_t* err_flag, void* stream);
 
 /*
- * moe_layer -- the whole layer: moe_gate_up then moe_down on `stream`.
+ * moe_layer -- the whole layer: the gate/up step then moe_down on `stream`.
+ * The gate/up step runs moe_gate_up's kernel, or moe_gate_up_grouped's when
+ * 2 * B * top_k >= 5 * E and that kernel takes the shape (see there).
  * h_scratch [B][top_k][I] BF16 is caller-provided device memory that holds
  * the intermediate between the two kernels (its contents afterwards are the
- * intermediate, as from moe_gate_up).
+ * intermediate, as from the gate/up kernel that ran).
  */
 moe_status moe_layer(const moe_shape* shape, const moe_weights* w, const uint16_t* x,
                      const int32_t* ids, const float* wts, int32_t B, uint16_t* h_scratch,
@@ -192,13 +194,17 @@ moe_status moe_route(const moe_shape* shape, const float* logits, int32_t B, int
 
 /*
  * moe_layer_routed -- the layer from router logits (the same choice as
- * moe_route). Two ways, the same results bit for bit:
+ * moe_route). Two ways, with the same results bit for bit below
+ * 2 * B * top_k = 5 * E:
  *  - ids_out and wts_out both non-NULL ([B][top_k], as moe_route): every token
- *    is routed once into them by the router kernel, and the two layer kernels
- *    read that routing. The faster way.
+ *    is routed once into them by the router kernel, and the layer reads that
+ *    routing exactly as moe_layer does (same choice of gate/up kernel). The
+ *    faster way.
  *  - both NULL: no ids/weights array exists at all. Every warp of moe_gate_up
  *    and moe_down routes its token from `logits` itself before it requests
- *    weights, which costs about 30 % of the layer at B=32.
+ *    weights, which costs about 30 % of the layer at B=32. This way always
+ *    uses moe_gate_up's per-token kernel, so from 2 * B * top_k >= 5 * E it
+ *    agrees with the other way to FP32 rounding order, not bit for bit.
  * Same limits as moe_route; other arguments as for moe_layer.
  */
 moe_status moe_layer_routed(const moe_shape* shape, const moe_weights* w, const uint16_t* x,
