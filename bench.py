@@ -97,7 +97,7 @@ def measured_peaks():
 
 KERNEL_SOURCES = {
     "moe_gate_up": ["wd_device.cuh", "wd_gate_up.cuh", "wd_gate_up.cu", "wd_gate_up_fixed.cu"],
-    "moe_gate_up_grouped": ["wd_device.cuh", "wd_gate_up_grouped.cu"],
+    "moe_gate_up_grouped": ["wd_device.cuh", "wd_gate_up_grouped.h", "wd_gate_up_grouped.cu"],
     "moe_down": ["wd_device.cuh", "wd_down.cu"],
 }
 

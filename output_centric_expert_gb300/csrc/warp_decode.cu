@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "wd_device.cuh"
+#include "wd_gate_up_grouped.h"
 
 namespace wd {
 

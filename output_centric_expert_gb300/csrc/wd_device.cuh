@@ -111,13 +111,6 @@ moe_status launch_gate_up_kernels(const moe_shape* s, const moe_weights* w, cons
 bool launch_gate_up_fixed_h(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                             const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
                             cudaStream_t st, RouteArgs route, int spw, moe_status* rc);
-// The expert-grouped moe_gate_up (wd_gate_up_grouped.cu): whether it handles
-// the shape and weights (H % 256 == 0, I % 64 == 0, 4-byte aligned scales),
-// and its launch (ids only, no routing from logits).
-bool gate_up_grouped_supported(const moe_shape* s, const moe_weights* w);
-moe_status launch_gate_up_grouped(const moe_shape* s, const moe_weights* w, const uint16_t* x,
-                                  const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
-                                  cudaStream_t st);
 // dependent = true launches moe_down as a programmatic dependent of the kernel
 // before it on the stream (used by the layer entry points, where that kernel
 // is moe_gate_up and only h is produced by it).

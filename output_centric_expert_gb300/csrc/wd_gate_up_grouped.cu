@@ -46,6 +46,7 @@
 // 17 tokens (Qwen-3-235B-A22B shape) under uniform routing, and at 32 tokens
 // under skewed routing.
 #include "wd_device.cuh"
+#include "wd_gate_up_grouped.h"
 
 namespace wd {
 namespace {
