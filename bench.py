@@ -420,8 +420,8 @@ def run_ours(args, wl, rank, world, local_rank):
 
     # ---- per-kernel durations (same steps, an event between the kernels) --
     # the gate/up kernel the layer itself runs at this shape and batch
-    gu_kernel = "moe_gate_up_grouped" if ops.layer_gate_up_kernel(layers[0].shape, wl.B) == "grouped" \
-        else "moe_gate_up"
+    gu_form = ops.layer_gate_up_kernel(layers[0].shape, wl.B, layers[0])
+    gu_kernel = "moe_gate_up_grouped" if gu_form == "grouped" else "moe_gate_up"
     gate_up_fn = getattr(ops, gu_kernel)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     barrier()
@@ -637,7 +637,7 @@ def run_sweep(names, steps: int, gate_up_forms: bool = False):
                 forms[form] = {"us": round(f_us, 2), "gbs": round(gu_b / f_us / 1e3, 1)}
         print(json.dumps({"workload": name, "H": s.H, "I": s.I, "E": s.E, "top_k": s.top_k,
                           "B": wl.B, "routing": wl.routing,
-                          "gate_up_kernel": ops.layer_gate_up_kernel(layers[0].shape, wl.B),
+                          "gate_up_kernel": ops.layer_gate_up_kernel(layers[0].shape, wl.B, layers[0]),
                           "us_per_layer": round(us, 2),
                           "tokens_per_s": round(wl.B / us * 1e6), "unique_experts": uniq,
                           "layer_bytes": lay_bytes, "layer_gbs": round(lay_bytes / us / 1e3, 1),

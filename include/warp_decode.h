@@ -140,6 +140,19 @@ moe_status moe_gate_up_grouped(const moe_shape* shape, const moe_weights* w,
                                int32_t* err_flag, void* stream);
 
 /*
+ * moe_layer_gate_up_kernel -- which kernel the layer entry points (moe_layer,
+ * moe_layer_host, moe_layer_noalloc, moe_layer_routed with ids_out) run for
+ * the gate/up step of a batch of B tokens: *kernel_out = 0 for moe_gate_up's
+ * per-token kernel, 1 for moe_gate_up_grouped's. A token's results can differ
+ * in FP32 rounding order between the two, never beyond that. `w` may be NULL,
+ * in which case gu_scales is taken to be suitably aligned. Host-only (no
+ * device call); returns MOE_ERR_SHAPE / MOE_ERR_NULL for a bad shape or a
+ * NULL shape or kernel_out.
+ */
+moe_status moe_layer_gate_up_kernel(const moe_shape* shape, const moe_weights* w, int32_t B,
+                                    int32_t* kernel_out);
+
+/*
  * moe_down -- second kernel ("moe_down_3d_batched" on the pages).
  *   h    [B][top_k][I] BF16 intermediate from moe_gate_up (device)
  *   ids  [B][top_k]    int32 expert ids (device)

@@ -145,7 +145,7 @@ moe_status gate_up_impl(const moe_shape* s, const moe_weights* w, const uint16_t
 // the Qwen-3-235B-A22B shape (1.06 E): each weight is decoded once rather
 // than once per routed pair.
 GateUpForm layer_form(const moe_shape* s, const moe_weights* w, int32_t B) {
-  if (s && w && 2 * (int64_t)B * s->top_k >= 5 * (int64_t)s->E && gate_up_grouped_supported(s, w))
+  if (s && 2 * (int64_t)B * s->top_k >= 5 * (int64_t)s->E && gate_up_grouped_supported(s, w))
     return GateUpForm::kGrouped;
   return GateUpForm::kPerToken;
 }
@@ -184,6 +184,16 @@ extern "C" moe_status moe_gate_up_grouped(const moe_shape* shape, const moe_weig
   using namespace wd;
   return gate_up_impl(shape, w, x, ids, B, h, err_flag, (cudaStream_t)stream, kNoRoute,
                       GateUpForm::kGrouped);
+}
+
+extern "C" moe_status moe_layer_gate_up_kernel(const moe_shape* shape, const moe_weights* w,
+                                               int32_t B, int32_t* kernel_out) {
+  using namespace wd;
+  if (!kernel_out) return MOE_ERR_NULL;
+  const moe_status rc = check_shape(shape, B);
+  if (rc != MOE_OK) return rc;
+  *kernel_out = layer_form(shape, w, B) == GateUpForm::kGrouped ? 1 : 0;
+  return MOE_OK;
 }
 
 extern "C" moe_status moe_down(const moe_shape* shape, const moe_weights* w, const uint16_t* h,

@@ -295,7 +295,8 @@ constexpr int kGrpUnroll = 8;
 }  // namespace
 
 bool gate_up_grouped_supported(const moe_shape* s, const moe_weights* w) {
-  return s->H % (32 * kGrpUnroll) == 0 && s->I % kGrpNeurons == 0 && aligned(w->gu_scales, 8) &&
+  return s->H % (32 * kGrpUnroll) == 0 && s->I % kGrpNeurons == 0 &&
+         (w == nullptr || aligned(w->gu_scales, 8)) &&
          (size_t)kGrpCols * grp_row_bytes(s->H) <= kMaxDynSmem &&
          (int64_t)s->E * (s->I / kGrpNeurons) <= 0x7FFFFFFF;
 }

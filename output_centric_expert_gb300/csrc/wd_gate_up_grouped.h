@@ -9,7 +9,8 @@
 namespace wd {
 
 // Whether the grouped kernel handles the shape and weights: H % 256 == 0,
-// I % 64 == 0, gu_scales 8-byte aligned, and the grid within CUDA's limit.
+// I % 64 == 0, gu_scales 8-byte aligned (not checked when w is NULL), and the
+// grid within CUDA's limit.
 bool gate_up_grouped_supported(const moe_shape* s, const moe_weights* w);
 
 // Launch it on `st` (expert ids only, no routing from logits); the arguments

@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         L.moe_gate_up.argtypes = [sp, wp, vp, vp, i32, vp, vp, vp]
         L.moe_gate_up_grouped.restype = ctypes.c_int
         L.moe_gate_up_grouped.argtypes = [sp, wp, vp, vp, i32, vp, vp, vp]
+        L.moe_layer_gate_up_kernel.restype = ctypes.c_int
+        L.moe_layer_gate_up_kernel.argtypes = [sp, wp, i32, ctypes.POINTER(ctypes.c_int32)]
         L.moe_down.restype = ctypes.c_int
         L.moe_down.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp]
         L.moe_layer.restype = ctypes.c_int
@@ -193,15 +195,16 @@ def moe_gate_up_grouped(weights: DeviceWeights, x: torch.Tensor, ids: torch.Tens
     return h
 
 
-def layer_gate_up_kernel(shape: MoeShape, B: int) -> str:
-    """The moe_gate_up kernel the layer entry points run for `shape` at batch B,
-    by the library's rule: "grouped" (moe_gate_up_grouped's) once
-    2 * B * top_k >= 5 * E when that kernel takes the shape (H % 256 == 0,
-    I % 64 == 0), else "per_token" (moe_gate_up's). Scales are assumed 8-byte
-    aligned, as DeviceWeights allocates them."""
-    if (2 * B * shape.top_k >= 5 * shape.E and shape.H % 256 == 0 and shape.I % 64 == 0):
-        return "grouped"
-    return "per_token"
+def layer_gate_up_kernel(shape: MoeShape, B: int, weights: "DeviceWeights | None" = None) -> str:
+    """The gate/up kernel the layer entry points run at batch B, as the library
+    reports it (moe_layer_gate_up_kernel): "per_token" (moe_gate_up's) or
+    "grouped" (moe_gate_up_grouped's). Without `weights` the scales are taken
+    to be aligned, as DeviceWeights allocates them."""
+    out = ctypes.c_int32(-1)
+    _check("moe_layer_gate_up_kernel", lib().moe_layer_gate_up_kernel(
+        ctypes.byref(shape), ctypes.byref(weights.struct) if weights is not None else None, B,
+        ctypes.byref(out)))
+    return "grouped" if out.value == 1 else "per_token"
 
 
 def moe_down(weights: DeviceWeights, h: torch.Tensor, ids: torch.Tensor, wts: torch.Tensor,
@@ -295,6 +298,6 @@ def moe_layer_host(weights: DeviceWeights, x_host: torch.Tensor, ids_host: torch
 def exported_symbols() -> list[str]:
     """The entry points include/warp_decode.h declares."""
     return ["moe_packed_bytes", "moe_pack_weights", "moe_gate_up", "moe_gate_up_grouped",
-            "moe_down", "moe_layer",
+            "moe_layer_gate_up_kernel", "moe_down", "moe_layer",
             "moe_layer_host", "moe_layer_noalloc", "moe_route", "moe_layer_routed",
             "moe_status_string", "moe_last_error"]

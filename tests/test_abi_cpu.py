@@ -140,7 +140,7 @@ C_CLIENT = r"""
 typedef void (*any_fn)(void);
 static const any_fn entry_points[] = {
   (any_fn)moe_packed_bytes, (any_fn)moe_pack_weights, (any_fn)moe_gate_up,
-  (any_fn)moe_gate_up_grouped, (any_fn)moe_down,
+  (any_fn)moe_gate_up_grouped, (any_fn)moe_layer_gate_up_kernel, (any_fn)moe_down,
   (any_fn)moe_layer, (any_fn)moe_layer_host, (any_fn)moe_route, (any_fn)moe_layer_routed,
   (any_fn)moe_layer_noalloc, (any_fn)moe_status_string, (any_fn)moe_last_error,
 };
@@ -183,9 +183,11 @@ def test_header_is_plain_c_and_links(tmp_path):
 
 
 def test_layer_gate_up_kernel_rule():
-    """The binding's statement of the layer's kernel choice: the grouped kernel
-    from 2*B*top_k >= 5E when it takes the shape (the GPU test
-    test_layer_uses_the_grouped_kernel_from_2_5e_pairs checks the library)."""
+    """The library's statement of the layer's gate/up kernel (a host-only call):
+    the grouped kernel from 2*B*top_k >= 5E when it takes the shape (H % 256,
+    I % 64), the per-token kernel otherwise. The GPU test
+    test_layer_uses_the_grouped_kernel_from_2_5e_pairs checks that the layer
+    really runs the kernel reported here."""
     q30 = ops.make_shape(2048, 768, 128, 8)
     assert ops.layer_gate_up_kernel(q30, 39) == "per_token"
     assert ops.layer_gate_up_kernel(q30, 40) == "grouped"
@@ -193,3 +195,16 @@ def test_layer_gate_up_kernel_rule():
     assert ops.layer_gate_up_kernel(ops.make_shape(2048, 96, 128, 8), 64) == "per_token"
     assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 9) == "per_token"
     assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 10) == "grouped"
+    for (H, I, E, k) in [(2048, 768, 128, 8), (4096, 1536, 128, 8), (7168, 2048, 256, 8),
+                         (4096, 14336, 8, 2), (256, 128, 8, 2), (768, 192, 5, 3)]:
+        sh = ops.make_shape(H, I, E, k)
+        for B in (1, 2, 5, 16, 17, 39, 40, 64, 65, 256):
+            want = "grouped" if (2 * B * k >= 5 * E and H % 256 == 0 and I % 64 == 0) else "per_token"
+            assert ops.layer_gate_up_kernel(sh, B) == want, (H, I, E, k, B)
+    # misaligned scales keep the per-token kernel; a bad shape is an error
+    w = ops.MoeWeights(256, 0x1001, 256, 256)
+    out = ctypes.c_int32(-1)
+    assert ops.lib().moe_layer_gate_up_kernel(ctypes.byref(q30), ctypes.byref(w), 64,
+                                              ctypes.byref(out)) == 0 and out.value == 0
+    with pytest.raises(ops.WarpDecodeError):
+        ops.layer_gate_up_kernel(ops.make_shape(100, 768, 128, 8), 64)
