@@ -15,6 +15,11 @@
  *                 streamed over all top-k experts' down rows with the routing
  *                 weight folded in, then reduced across the 32 lanes by a
  *                 butterfly shuffle. No per-expert output buffer exists.
+ * For batches where many routed pairs share each expert (2 * B * top_k >=
+ * 5 * E), the layer computes the gate/up step with an expert-grouped kernel
+ * instead (moe_gate_up_grouped: one warp per (expert, 8 neurons) for all the
+ * pairs routed to that expert, multiplying on tensor cores); each
+ * intermediate is still written once by one warp, with the same numerics.
  *
  * Numerics (fixed by this API):
  *   g = sum_h x[t,h] Wg[e,n,h],  u = sum_h x[t,h] Wu[e,n,h]     (FP32 accum.)
