@@ -150,9 +150,10 @@ moe_status moe_gate_up_grouped(const moe_shape* shape, const moe_weights* w,
  * the gate/up step of a batch of B tokens: *kernel_out = 0 for moe_gate_up's
  * per-token kernel, 1 for moe_gate_up_grouped's. A token's results can differ
  * in FP32 rounding order between the two, never beyond that. `w` may be NULL,
- * in which case gu_scales is taken to be suitably aligned. Host-only (no
- * device call); returns MOE_ERR_SHAPE / MOE_ERR_NULL for a bad shape or a
- * NULL shape or kernel_out.
+ * in which case gu_scales is taken to be suitably aligned; a non-NULL `w` has
+ * its gate/up arrays checked as the layer entry points check them. Host-only
+ * (no device call); returns MOE_ERR_SHAPE / MOE_ERR_NULL / MOE_ERR_ALIGN for a
+ * bad shape, a NULL shape, kernel_out or gate/up array, or misaligned codes.
  */
 moe_status moe_layer_gate_up_kernel(const moe_shape* shape, const moe_weights* w, int32_t B,
                                     int32_t* kernel_out);
@@ -168,6 +169,44 @@ moe_status moe_layer_gate_up_kernel(const moe_shape* shape, const moe_weights* w
 moe_status moe_down(const moe_shape* shape, const moe_weights* w, const uint16_t* h,
                     const int32_t* ids, const float* wts, int32_t B, float* y,
                     int32_t* err_flag, void* stream);
+
+/*
+ * moe_down_grouped -- moe_down computed by its expert-grouped kernel: one CTA
+ * per 16 output rows o0..o0+15 serves every token of the batch. Its 8 warps
+ * take the batch's routed experts in turn; for each, a warp streams rows
+ * o0..o0+15 of that expert's down matrix once and multiplies them on the
+ * tensor cores (mma.sync m16n8k16, f16 operands, FP32 accumulation; rows are
+ * the 16 output dimensions, columns 8 of the pairs routed to the expert),
+ * each block sum times its E8M0 scale, then adds routing weight x sum into
+ * the warp's own partial sums of y in shared memory. The CTA adds its warps'
+ * partial sums in a fixed order and writes every y[t,o] once: no atomics, no
+ * per-expert output buffer, no combine in global memory ("Better MoE model
+ * inference with warp decode", [§How the two kernels work], [§Buffer
+ * elimination]); each down weight is decoded once per call instead of once
+ * per (token, slot). Arguments and result as for moe_down; the sums differ
+ * from moe_down's in FP32 rounding order, and a token's result can depend on
+ * which other tokens share the batch in that order only. Results are the same
+ * on every call with the same inputs. Returns MOE_ERR_UNSUPPORTED, launching
+ * nothing, unless I % 256 == 0, E <= 256, 1 <= B <= 128 (B == 0 is an empty
+ * batch), d_scales is 8-byte aligned and the batch's tables fit in one CTA's
+ * shared memory. The layer entry points use this kernel by themselves when
+ * B * top_k >= 3 * E and it takes the shape and batch (measured faster there
+ * on GB300; see moe_layer_down_kernel).
+ */
+moe_status moe_down_grouped(const moe_shape* shape, const moe_weights* w, const uint16_t* h,
+                            const int32_t* ids, const float* wts, int32_t B, float* y,
+                            int32_t* err_flag, void* stream);
+
+/*
+ * moe_layer_down_kernel -- which kernel the layer entry points (moe_layer,
+ * moe_layer_host, moe_layer_noalloc, moe_layer_routed with ids_out) run for
+ * the down step of a batch of B tokens: *kernel_out = 0 for moe_down's
+ * per-token kernel, 1 for moe_down_grouped's. Host-only; `w` may be NULL (the
+ * scales are then taken to be aligned); errors as for moe_layer_gate_up_kernel,
+ * with the down arrays of a non-NULL `w` checked.
+ */
+moe_status moe_layer_down_kernel(const moe_shape* shape, const moe_weights* w, int32_t B,
+                                 int32_t* kernel_out);
 
 /*
  * moe_layer -- the whole layer: the gate/up step then moe_down on `stream`.
@@ -241,7 +280,11 @@ moe_status moe_layer_routed(const moe_shape* shape, const moe_weights* w, const 
  *   returns MOE_ERR_SHAPE (moe_last_error() says why) before anything runs.
  *   The first call on each device looks up the array's device address with
  *   cudaGetSymbolAddress, with that device current; make that first call
- *   before any stream capture. The call allocates nothing.
+ *   before any stream capture. The call allocates nothing. The address is
+ *   kept for the rest of the process: after cudaDeviceReset on a device (which
+ *   unloads this library's device code there, so the array may come back at
+ *   another address) the kept address is stale, and this entry point must
+ *   not be called on that device again.
  *   All calls share the one array: calls whose work overlaps on the GPU (for
  *   example on two streams at once) race on it. Each call overwrites every
  *   value it reads, so nothing needs clearing between calls.

@@ -58,7 +58,7 @@ def _stale(target: str, sources: list[str]) -> bool:
 
 def _cuda_sources() -> list[str]:
     names = ["warp_decode.cu", "wd_gate_up.cu", "wd_gate_up_fixed.cu", "wd_gate_up_grouped.cu",
-             "wd_down.cu", "pack.cpp"]
+             "wd_down.cu", "wd_down_grouped.cu", "pack.cpp"]
     return [os.path.join(CSRC, n) for n in names]
 
 

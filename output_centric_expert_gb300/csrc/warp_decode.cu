@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "wd_device.cuh"
+#include "wd_down_grouped.h"
 #include "wd_gate_up_grouped.h"
 
 namespace wd {
@@ -150,12 +151,22 @@ GateUpForm layer_form(const moe_shape* s, const moe_weights* w, int32_t B) {
   return GateUpForm::kPerToken;
 }
 
+// Which kernel computes y: the per-token one of moe_down (outputs per warp
+// chosen by the batch) or the expert-grouped one.
+enum class DownForm { kPerToken, kGrouped };
+
 moe_status down_impl(const moe_shape* s, const moe_weights* w, const uint16_t* h,
                      const int32_t* ids, const float* wts, int32_t B, float* y, int32_t* err,
-                     cudaStream_t st, bool dependent, const float* logits = nullptr) {
+                     cudaStream_t st, bool dependent, const float* logits = nullptr,
+                     DownForm form = DownForm::kPerToken) {
   moe_status rc = check_shape(s, B);
   if (rc != MOE_OK) return rc;
   if ((rc = check_weights(w, false, true)) != MOE_OK) return rc;
+  if (form == DownForm::kGrouped && B > 0 && !down_grouped_supported(s, w, B)) {
+    set_error_msg("moe_down_grouped: needs I % 256 == 0, E <= 256, B <= 128, 8-byte aligned "
+                  "d_scales and the batch's tables within shared memory");
+    return MOE_ERR_UNSUPPORTED;
+  }
   if (B == 0) return MOE_OK;
   if (!h || ((!ids || !wts) && !logits) || !y) return MOE_ERR_NULL;
   if (!aligned(h, 16) || !aligned(ids, 4) || !aligned(wts, 4) || !aligned(y, 4) ||
@@ -163,9 +174,24 @@ moe_status down_impl(const moe_shape* s, const moe_weights* w, const uint16_t* h
     set_error_msg("alignment: h needs 16 bytes, ids/wts/y/err_flag 4");
     return MOE_ERR_ALIGN;
   }
-  rc = launch_down_kernels(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+  if (form == DownForm::kGrouped)
+    rc = launch_down_grouped(s, w, h, ids, wts, B, y, err, st, dependent);
+  else
+    rc = launch_down_kernels(s, w, h, ids, wts, B, y, err, st, dependent, logits);
   if (rc != MOE_OK) return rc;
   return launch_status("moe_down launch");
+}
+
+// The form of moe_down a layer entry point uses: the expert-grouped kernel once
+// B * top_k >= 3 * E, if it takes the shape and batch. Measured on GB300 (each
+// kernel alone, CUDA graph, cold L2), per-token vs grouped: Qwen-3-30B-A3B
+// shape 43.1 vs 46.4 us at 32 tokens (2 pairs per expert), 74.1 vs 66.3 at 64;
+// Qwen-3-235B-A22B shape 99.5 vs 117.4 at 16, 306.1 vs 241.8 at 64;
+// Mixtral-shaped (4 pairs per expert at 16 tokens) 210.0 vs 188.6.
+DownForm layer_down_form(const moe_shape* s, const moe_weights* w, int32_t B) {
+  if (s && (int64_t)B * s->top_k >= 3 * (int64_t)s->E && down_grouped_supported(s, w, B))
+    return DownForm::kGrouped;
+  return DownForm::kPerToken;
 }
 
 }  // namespace
@@ -190,8 +216,9 @@ extern "C" moe_status moe_layer_gate_up_kernel(const moe_shape* shape, const moe
                                                int32_t B, int32_t* kernel_out) {
   using namespace wd;
   if (!kernel_out) return MOE_ERR_NULL;
-  const moe_status rc = check_shape(shape, B);
+  moe_status rc = check_shape(shape, B);
   if (rc != MOE_OK) return rc;
+  if (w && (rc = check_weights(w, true, false)) != MOE_OK) return rc;
   *kernel_out = layer_form(shape, w, B) == GateUpForm::kGrouped ? 1 : 0;
   return MOE_OK;
 }
@@ -201,6 +228,25 @@ extern "C" moe_status moe_down(const moe_shape* shape, const moe_weights* w, con
                                int32_t* err_flag, void* stream) {
   using namespace wd;
   return down_impl(shape, w, h, ids, wts, B, y, err_flag, (cudaStream_t)stream, false);
+}
+
+extern "C" moe_status moe_down_grouped(const moe_shape* shape, const moe_weights* w,
+                                       const uint16_t* h, const int32_t* ids, const float* wts,
+                                       int32_t B, float* y, int32_t* err_flag, void* stream) {
+  using namespace wd;
+  return down_impl(shape, w, h, ids, wts, B, y, err_flag, (cudaStream_t)stream, false, nullptr,
+                   DownForm::kGrouped);
+}
+
+extern "C" moe_status moe_layer_down_kernel(const moe_shape* shape, const moe_weights* w,
+                                            int32_t B, int32_t* kernel_out) {
+  using namespace wd;
+  if (!kernel_out) return MOE_ERR_NULL;
+  moe_status rc = check_shape(shape, B);
+  if (rc != MOE_OK) return rc;
+  if (w && (rc = check_weights(w, false, true)) != MOE_OK) return rc;
+  *kernel_out = layer_down_form(shape, w, B) == DownForm::kGrouped ? 1 : 0;
+  return MOE_OK;
 }
 
 extern "C" moe_status moe_layer(const moe_shape* shape, const moe_weights* w, const uint16_t* x,
@@ -217,7 +263,8 @@ extern "C" moe_status moe_layer(const moe_shape* shape, const moe_weights* w, co
   rc = gate_up_impl(shape, w, x, ids, B, h_scratch, err_flag, (cudaStream_t)stream, kNoRoute,
                     layer_form(shape, w, B));
   if (rc != MOE_OK) return rc;
-  return down_impl(shape, w, h_scratch, ids, wts, B, y, err_flag, (cudaStream_t)stream, true);
+  return down_impl(shape, w, h_scratch, ids, wts, B, y, err_flag, (cudaStream_t)stream, true,
+                   nullptr, layer_down_form(shape, w, B));
 }
 
 extern "C" moe_status moe_route(const moe_shape* shape, const float* logits, int32_t B,
@@ -266,7 +313,8 @@ extern "C" moe_status moe_layer_routed(const moe_shape* shape, const moe_weights
     rc = gate_up_impl(shape, w, x, ids_out, B, h_scratch, err_flag, st, kNoRoute,
                       layer_form(shape, w, B));
     if (rc != MOE_OK) return rc;
-    return down_impl(shape, w, h_scratch, ids_out, wts_out, B, y, err_flag, st, true);
+    return down_impl(shape, w, h_scratch, ids_out, wts_out, B, y, err_flag, st, true, nullptr,
+                     layer_down_form(shape, w, B));
   }
   const RouteArgs route = {logits};
   rc = gate_up_impl(shape, w, x, nullptr, B, h_scratch, err_flag, st, route);
@@ -344,7 +392,8 @@ uint16_t* g_noalloc_ptr[kNoAllocMaxDevices] = {};
 // Device address of the fixed intermediate array on the current device. Host
 // code must not pass the array's name to a kernel (on the host it only stands
 // for the symbol), so the address is looked up once per device, with that
-// device current, and cached.
+// device current, and cached for the rest of the process (a cudaDeviceReset
+// makes the cached address stale; the header says so).
 moe_status noalloc_intermediate(uint16_t** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -397,5 +446,6 @@ extern "C" moe_status moe_layer_noalloc(const moe_shape* shape, const moe_weight
   rc = gate_up_impl(shape, w, x, ids, B, h, err_flag, (cudaStream_t)stream, kNoRoute,
                     layer_form(shape, w, B));
   if (rc != MOE_OK) return rc;
-  return down_impl(shape, w, h, ids, wts, B, y, err_flag, (cudaStream_t)stream, true);
+  return down_impl(shape, w, h, ids, wts, B, y, err_flag, (cudaStream_t)stream, true, nullptr,
+                   layer_down_form(shape, w, B));
 }

@@ -60,31 +60,6 @@ constexpr int kGrpCols = 8;                                      // pairs per MM
 // warp (two tokens x four lanes) hit distinct banks.
 __host__ __device__ constexpr int grp_row_bytes(int H) { return 2 * H + 64; }
 
-// d = a * b + c for one m16n8k16 tile: f16 operands, FP32 accumulate.
-__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                          uint32_t b1, const float (&c)[4]) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%10,%11,%12,%13};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
-        "f"(c[2]), "f"(c[3]));
-}
-
-// 16 codes (half of one of two adjacent 32-element blocks), not allocated in L1.
-__device__ __forceinline__ uint4 ld_codes16(const uint8_t* p) {
-  uint4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
-  return r;
-}
-// The E8M0 scales of 8 consecutive blocks of one row.
-__device__ __forceinline__ uint2 ld_scales8(const uint8_t* p) {
-  uint2 r;
-  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-  return r;
-}
-
 // UNR: 32-element blocks per loop step (a multiple of 8: one 64-bit load of
 // scales per row per 8 blocks). NCH: column tiles of 8 pairs held at once.
 template <int UNR>

@@ -59,6 +59,10 @@ def lib() -> ctypes.CDLL:
         L.moe_layer_gate_up_kernel.argtypes = [sp, wp, i32, ctypes.POINTER(ctypes.c_int32)]
         L.moe_down.restype = ctypes.c_int
         L.moe_down.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp]
+        L.moe_down_grouped.restype = ctypes.c_int
+        L.moe_down_grouped.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp]
+        L.moe_layer_down_kernel.restype = ctypes.c_int
+        L.moe_layer_down_kernel.argtypes = [sp, wp, i32, ctypes.POINTER(ctypes.c_int32)]
         L.moe_layer.restype = ctypes.c_int
         L.moe_layer.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp, vp]
         L.moe_route.restype = ctypes.c_int
@@ -219,6 +223,31 @@ def moe_down(weights: DeviceWeights, h: torch.Tensor, ids: torch.Tensor, wts: to
     return y
 
 
+def moe_down_grouped(weights: DeviceWeights, h: torch.Tensor, ids: torch.Tensor,
+                     wts: torch.Tensor, y: torch.Tensor, err_flag: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """moe_down by the expert-grouped kernel (each down weight decoded once,
+    tensor-core MMAs over the pairs routed to each expert); same result up to
+    FP32 rounding order."""
+    B = ids.shape[0]
+    _check("moe_down_grouped", lib().moe_down_grouped(
+        ctypes.byref(weights.shape), ctypes.byref(weights.struct), _ptr(h, _BF16, "h"),
+        _ptr(ids, (torch.int32,), "ids"), _ptr(wts, (torch.float32,), "wts"), B,
+        _ptr(y, (torch.float32,), "y"), _ptr(err_flag, (torch.int32,), "err_flag"),
+        _stream(stream)))
+    return y
+
+
+def layer_down_kernel(shape: MoeShape, B: int, weights: "DeviceWeights | None" = None) -> str:
+    """The down kernel the layer entry points run at batch B, as the library
+    reports it (moe_layer_down_kernel): "per_token" or "grouped"."""
+    out = ctypes.c_int32(-1)
+    _check("moe_layer_down_kernel", lib().moe_layer_down_kernel(
+        ctypes.byref(shape), ctypes.byref(weights.struct) if weights is not None else None, B,
+        ctypes.byref(out)))
+    return "grouped" if out.value == 1 else "per_token"
+
+
 def moe_layer(weights: DeviceWeights, x: torch.Tensor, ids: torch.Tensor, wts: torch.Tensor,
               h_scratch: torch.Tensor, y: torch.Tensor, err_flag: torch.Tensor | None = None,
               stream=None) -> torch.Tensor:
@@ -298,6 +327,7 @@ def moe_layer_host(weights: DeviceWeights, x_host: torch.Tensor, ids_host: torch
 def exported_symbols() -> list[str]:
     """The entry points include/warp_decode.h declares."""
     return ["moe_packed_bytes", "moe_pack_weights", "moe_gate_up", "moe_gate_up_grouped",
-            "moe_layer_gate_up_kernel", "moe_down", "moe_layer",
+            "moe_layer_gate_up_kernel", "moe_down", "moe_down_grouped",
+            "moe_layer_down_kernel", "moe_layer",
             "moe_layer_host", "moe_layer_noalloc", "moe_route", "moe_layer_routed",
             "moe_status_string", "moe_last_error"]

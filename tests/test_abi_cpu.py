@@ -141,7 +141,7 @@ typedef void (*any_fn)(void);
 static const any_fn entry_points[] = {
   (any_fn)moe_packed_bytes, (any_fn)moe_pack_weights, (any_fn)moe_gate_up,
   (any_fn)moe_gate_up_grouped, (any_fn)moe_layer_gate_up_kernel, (any_fn)moe_down,
-  (any_fn)moe_layer, (any_fn)moe_layer_host, (any_fn)moe_route, (any_fn)moe_layer_routed,
+  (any_fn)moe_down_grouped, (any_fn)moe_layer_down_kernel, (any_fn)moe_layer, (any_fn)moe_layer_host, (any_fn)moe_route, (any_fn)moe_layer_routed,
   (any_fn)moe_layer_noalloc, (any_fn)moe_status_string, (any_fn)moe_last_error,
 };
 
@@ -208,3 +208,33 @@ def test_layer_gate_up_kernel_rule():
                                               ctypes.byref(out)) == 0 and out.value == 0
     with pytest.raises(ops.WarpDecodeError):
         ops.layer_gate_up_kernel(ops.make_shape(100, 768, 128, 8), 64)
+
+
+def test_layer_down_kernel_choice():
+    """The layer's down kernel: the expert-grouped one from B * top_k >= 3E when
+    it takes the shape (I % 256 == 0, E <= 256) and batch (up to 64 tokens for
+    these shapes; never beyond 128), the per-token one otherwise; the library
+    answers on the host, without a GPU."""
+    for (H, I, E, k) in [(2048, 768, 128, 8), (4096, 1536, 128, 8), (7168, 2048, 256, 8),
+                         (4096, 14336, 8, 2), (256, 128, 8, 2), (64, 256, 6, 3),
+                         (2048, 768, 257, 8)]:
+        sh = ops.make_shape(H, I, E, k)
+        for B in (1, 2, 3, 15, 16, 17, 32, 47, 48, 64, 129, 256):
+            want = "grouped" if (B * k >= 3 * E and I % 256 == 0 and E <= 256 and B <= 64) \
+                else "per_token"
+            assert ops.layer_down_kernel(sh, B) == want, (H, I, E, k, B)
+    # misaligned down scales keep the per-token kernel; NULL weight arrays and
+    # a bad shape are errors
+    q30 = ops.make_shape(2048, 768, 128, 8)
+    out = ctypes.c_int32(-1)
+    w = ops.MoeWeights(256, 256, 256, 0x1001)
+    assert ops.lib().moe_layer_down_kernel(ctypes.byref(q30), ctypes.byref(w), 64,
+                                           ctypes.byref(out)) == 0 and out.value == 0
+    w = ops.MoeWeights(256, 256, 256, None)
+    assert ops.lib().moe_layer_down_kernel(ctypes.byref(q30), ctypes.byref(w), 64,
+                                           ctypes.byref(out)) == 1
+    w = ops.MoeWeights(256, None, 256, 256)
+    assert ops.lib().moe_layer_gate_up_kernel(ctypes.byref(q30), ctypes.byref(w), 64,
+                                              ctypes.byref(out)) == 1
+    with pytest.raises(ops.WarpDecodeError):
+        ops.layer_down_kernel(ops.make_shape(100, 768, 128, 8), 64)
