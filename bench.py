@@ -47,10 +47,15 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="q30_b32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="leave out the B=1..64 sweep and accuracy keys of the contract line")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work the oracle baseline sample aims at")
     ap.add_argument("--gate-up-forms", action="store_true",
                     help="with --sweep: also time moe_gate_up and moe_gate_up_grouped alone "
+                         "(CUDA graph, same rotation) for every workload")
+    ap.add_argument("--down-forms", action="store_true",
+                    help="with --sweep: also time moe_down and moe_down_grouped alone "
                          "(CUDA graph, same rotation) for every workload")
     ap.add_argument("--sweep", nargs="*", default=None,
                     help="instead of the single contract line, print one line per workload "
@@ -404,15 +409,19 @@ def run_ours(args, wl, rank, world, local_rank):
             step(i)
         barrier()
         # ---- main timed region: K whole-layer steps ----------------------
+        step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
         barrier()
         wall0 = time.time()
         ev0.record(stream)
+        step_ev[0].record(stream)
         for i in range(args.steps):
             step(i)
+            step_ev[i + 1].record(stream)
         ev1.record(stream)
         barrier()
         wall1 = time.time()
     el_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    step_ms = sorted(step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps))
     ms_per_step = el_ms / args.steps
     value = job_tokens_per_s(wl.B, world, args.steps, el_ms)
     if int(err.item()) != 0:
@@ -501,6 +510,9 @@ def run_ours(args, wl, rank, world, local_rank):
         v, sample, cores = oracle_baseline_all_cores(wl, args.cpu_seconds)
         cpu_all = {"value": v, "unit": "tokens/s", "cores": cores,
                    "kind": "oracle, one token per thread", "sample": sample}
+    sweep = acc = None
+    if not args.no_sweep:
+        sweep, acc = metric_sweep(layers, dev, peak)
     traffic = ncu_traffic(gu_kernel, wl.name)
     gu_launch_bytes = sum(gu_bytes) / args.steps
     out = {
@@ -534,10 +546,149 @@ def run_ours(args, wl, rank, world, local_rank):
                               "unit": "tokens/s",
                               "how": "moe_layer_host on 2 streams taking alternate steps; one "
                                      "step's copies and kernels overlap the other's"}},
+        "step_ms": {"median": statistics.median(step_ms), "p90": step_ms[int(0.9 * (len(step_ms) - 1))],
+                    "min": step_ms[0], "max": step_ms[-1], "how": "CUDA events between the timed steps"},
+        "sweep": sweep,
+        "accuracy": acc,
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(wall0, wall1),
     }
     print(json.dumps(out), flush=True)
+
+
+def graph_layer_us(layers, dx, dids, dw, h, y, reps: int) -> float:
+    """moe_layer captured in one CUDA graph over a rotation of the layers and
+    token batches (step i: layer i % len(layers), batch i % len(dx)), replayed
+    `reps` times; CUDA-event microseconds per step. Launch overhead of the host
+    is outside the measurement, as in a graph-driven decode loop."""
+    import torch
+
+    from output_centric_expert_gb300 import ops
+    dev = dx[0].device
+    rot = 2 * len(dx)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for i in range(rot):  # warm-up outside capture
+            ops.moe_layer(layers[i % len(layers)], dx[i % len(dx)], dids[i % len(dx)],
+                          dw[i % len(dx)], h, y)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(rot):
+            ops.moe_layer(layers[i % len(layers)], dx[i % len(dx)], dids[i % len(dx)],
+                          dw[i % len(dx)], h, y)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) * 1e3 / (reps * rot)
+
+
+# The pages' metric covers B=1..64 ("Better MoE model inference with warp
+# decode", [§Hardware Efficiency]: accuracy "across all batch sizes"); the
+# default run times every point of the batch sweep and the larger layer, and
+# checks each against the oracle.
+METRIC_SWEEP = ([("q30", B, r) for r in ("uniform", "skewed") for B in (1, 2, 4, 8, 16, 32, 64)]
+                + [("q235", B, "uniform") for B in (1, 16, 64)])
+ACCURACY_TOKENS = {"q30": 4, "q235": 2}  # oracle tokens per point (first, last, evenly between)
+
+
+def metric_sweep(q30_layers, dev, peak, reps: int = 6):
+    """Every point of METRIC_SWEEP: the layer's time (graph_layer_us over 8
+    token batches and the layers given: the bench's two Qwen-3-30B-A3B-shaped
+    layers, one Qwen-3-235B-A22B-shaped layer of 2.5 GB, both far above L2), and
+    the achieved max |y - y_oracle| and minimum per-token cosine on sampled
+    tokens of the point's first batch. The oracle runs on the host cores, one
+    token per thread. Returns (sweep, accuracy) dicts for the JSON line."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import torch
+
+    import oracle
+    from output_centric_expert_gb300 import ops, workload
+    t_start = time.time()
+    points, checks = [], []
+    oracle_jobs = []
+    for name in ("q30", "q235"):
+        s = workload.SHAPES[name]
+        if name == "q30":
+            layers = q30_layers
+        else:
+            torch.cuda.empty_cache()
+            layers = build_device_layers(s, 1, 0, dev)
+        todo = [(B, r) for (n, B, r) in METRIC_SWEEP if n == name]
+        all_batches = {}
+        need = set()
+        for B, r in todo:
+            wl = workload.Workload(f"{name}_{r}_b{B}", s, B, r)
+            bs = make_batches(wl, N_BATCHES, 0)
+            all_batches[(B, r)] = (wl, bs)
+            smp = sorted(set(np.linspace(0, B - 1, min(B, ACCURACY_TOKENS[name])).round().astype(int)))
+            need |= set(bs[0][1][smp].ravel().tolist())
+        ref = _oracle_layer(s, 0, 0, sorted(need))
+        for B, r in todo:
+            wl, bs = all_batches[(B, r)]
+            dx = [torch.from_numpy(b[0].view(np.int16)).to(dev) for b in bs]
+            dids = [torch.from_numpy(b[1]).to(dev) for b in bs]
+            dw = [torch.from_numpy(b[2]).to(dev) for b in bs]
+            h = torch.empty((B, s.top_k, s.I), dtype=torch.int16, device=dev)
+            y = torch.empty((B, s.H), dtype=torch.float32, device=dev)
+            us = graph_layer_us(layers, dx, dids, dw, h, y, reps)
+            lay_bytes = float(np.mean([layer_bytes(s, b[1]) for b in bs]))
+            points.append({"workload": wl.name, "B": B, "routing": r, "us": round(us, 2),
+                           "tokens_per_s": round(B / us * 1e6),
+                           "gbs": round(lay_bytes / us / 1e3, 1),
+                           "frac_of_peak": round(lay_bytes / us / 1e3 / peak, 4),
+                           "unique_experts": float(np.mean([len(np.unique(b[1])) for b in bs])),
+                           "gate_up_kernel": ops.layer_gate_up_kernel(layers[0].shape, B, layers[0]),
+                           "down_kernel": ops.layer_down_kernel(layers[0].shape, B, layers[0])})
+            # accuracy: the first batch once more, eagerly, against the oracle
+            ops.moe_layer(layers[0], dx[0], dids[0], dw[0], h, y)
+            torch.cuda.synchronize(dev)
+            yg = y.cpu().numpy().astype(np.float64)
+            x, ids, w = bs[0]
+            smp = sorted(set(np.linspace(0, B - 1, min(B, ACCURACY_TOKENS[name])).round().astype(int)))
+            for t in smp:
+                oracle_jobs.append((wl.name, t, yg[t], ref, x[t:t + 1], ids[t:t + 1], w[t:t + 1]))
+        del layers
+    # one call before any thread starts: the oracle fills its decode tables on
+    # first use, and thread creation orders that before every worker's reads
+    _, _, _, ref0, x0, ids0, w0 = oracle_jobs[0]
+    oracle.moe_layer(ref0, x0, ids0, w0)
+
+    def one(job):
+        name, t, yt, ref, x, ids, w = job
+        yo, _ = oracle.moe_layer(ref, x, ids, w)
+        yo = yo[0]
+        d = float(np.max(np.abs(yt - yo)))
+        cos = float(np.dot(yt, yo) / (np.linalg.norm(yt) * np.linalg.norm(yo)))
+        return name, d, cos
+    with ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as ex:
+        res = list(ex.map(one, oracle_jobs))
+    per = {}
+    for name, d, cos in res:
+        a = per.setdefault(name, {"workload": name, "tokens": 0, "max_abs": 0.0, "min_cos": 1.0})
+        a["tokens"] += 1
+        a["max_abs"] = max(a["max_abs"], d)
+        a["min_cos"] = min(a["min_cos"], cos)
+    checks = list(per.values())
+    sweep = {"timing": f"CUDA graph of 16 steps over 8 token batches and the layers (Q30: 2 layers, "
+                       f"Q235: 1 layer of 2.5 GB), replayed {reps} times; cold L2",
+             "peak_gbs": peak, "points": points}
+    acc = {"vs": "FP64 CPU oracle on the same packed weights",
+           "points": checks, "max_abs": max(c["max_abs"] for c in checks),
+           "min_cos": min(c["min_cos"] for c in checks),
+           "bar": {"max_abs": 4e-3, "min_cos": 0.99999},
+           "pages_b200_context": {"max_abs": 0.001953, "min_cos": 0.999996},
+           "seconds": round(time.time() - t_start, 1)}
+    return sweep, acc
 
 
 SWEEP_DEFAULT = ([f"q30_{r}_b{b}" for r in ("uniform", "skewed") for b in (1, 2, 4, 8, 16, 32, 64)]
@@ -545,7 +696,7 @@ SWEEP_DEFAULT = ([f"q30_{r}_b{b}" for r in ("uniform", "skewed") for b in (1, 2,
 SWEEP_VARIANTS = ["dsv3_b1", "dsv3_b16", "dsv3_b64", "mixtral_b1", "mixtral_b16", "mixtral_b64"]
 
 
-def run_sweep(names, steps: int, gate_up_forms: bool = False):
+def run_sweep(names, steps: int, gate_up_forms: bool = False, down_forms: bool = False):
     """Per workload: the layer (moe_layer, both kernels) captured in a CUDA graph
     over a rotation of 2 layers x 8 token batches, replayed; CUDA-event time per
     step. Launch overhead of the host is outside the measurement, as in a
@@ -635,9 +786,42 @@ def run_sweep(names, steps: int, gate_up_forms: bool = False):
                 torch.cuda.synchronize(dev)
                 f_us = e0.elapsed_time(e1) * 1e3 / (reps * rot)
                 forms[form] = {"us": round(f_us, 2), "gbs": round(gu_b / f_us / 1e3, 1)}
+        down = {}
+        if down_forms:
+            # each down kernel alone over the same rotation, fed each batch's
+            # intermediate; GB/s of its own bytes
+            hs = []
+            for b in range(N_BATCHES):
+                hb = torch.empty_like(h)
+                ops.moe_gate_up(layers[0], dx[b], dids[b], hb)
+                hs.append(hb)
+            dn_b = float(np.mean([down_bytes(s, b[1]) for b in batches]))
+            for form, fn in (("per_token", ops.moe_down), ("grouped", ops.moe_down_grouped)):
+                try:  # the grouped kernel refuses some shapes and batches
+                    fn(layers[0], hs[0], dids[0], dw[0], y)
+                except ops.WarpDecodeError:
+                    continue
+                torch.cuda.synchronize(dev)
+                gf = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gf):
+                    for i in range(rot):
+                        fn(layers[i % N_LAYERS], hs[i % N_BATCHES], dids[i % N_BATCHES],
+                           dw[i % N_BATCHES], y)
+                for _ in range(2):
+                    gf.replay()
+                torch.cuda.synchronize(dev)
+                e0.record()
+                for _ in range(reps):
+                    gf.replay()
+                e1.record()
+                torch.cuda.synchronize(dev)
+                f_us = e0.elapsed_time(e1) * 1e3 / (reps * rot)
+                down[form] = {"us": round(f_us, 2), "gbs": round(dn_b / f_us / 1e3, 1),
+                              "frac_of_measured_peak": round(dn_b / f_us / 1e3 / peak, 4)}
         print(json.dumps({"workload": name, "H": s.H, "I": s.I, "E": s.E, "top_k": s.top_k,
                           "B": wl.B, "routing": wl.routing,
                           "gate_up_kernel": ops.layer_gate_up_kernel(layers[0].shape, wl.B, layers[0]),
+                          "down_kernel": ops.layer_down_kernel(layers[0].shape, wl.B, layers[0]),
                           "us_per_layer": round(us, 2),
                           "tokens_per_s": round(wl.B / us * 1e6), "unique_experts": uniq,
                           "layer_bytes": lay_bytes, "layer_gbs": round(lay_bytes / us / 1e3, 1),
@@ -645,14 +829,15 @@ def run_sweep(names, steps: int, gate_up_forms: bool = False):
                           "timing": "CUDA graph of 16 steps (2 layers x 8 batches), replayed",
                           "warm_l2_us_per_layer": round(warm_us, 2),
                           "warm_l2_bytes_per_layer": layer_bytes(s, batches[0][1]),
-                          **({"gate_up_alone": forms} if gate_up_forms else {})}),
+                          **({"gate_up_alone": forms} if gate_up_forms else {}),
+                          **({"down_alone": down} if down_forms else {})}),
               flush=True)
 
 
 def main():
     args = parse()
     if args.sweep is not None:
-        run_sweep(args.sweep or SWEEP_DEFAULT, args.steps, args.gate_up_forms)
+        run_sweep(args.sweep or SWEEP_DEFAULT, args.steps, args.gate_up_forms, args.down_forms)
         return
     from output_centric_expert_gb300 import workload
     wl = workload.WORKLOADS[args.workload]
