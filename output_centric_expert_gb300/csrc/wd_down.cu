@@ -22,6 +22,18 @@ struct DownUnit {
   uint32_t s[OPW];
 };
 
+// The unit's OPW block scales as FP32, two per hardware conversion.
+template <int OPW>
+__device__ __forceinline__ void unit_scales(const DownUnit<OPW>& U, float (&sc)[OPW]) {
+  if constexpr (OPW == 1) {
+    float unused;
+    e8m0x2_to_f32(U.s[0], 0u, sc[0], unused);
+  } else {
+#pragma unroll
+    for (int r = 0; r < OPW; r += 2) e8m0x2_to_f32(U.s[r], U.s[r + 1], sc[r], sc[r + 1]);
+  }
+}
+
 // UPL: units each lane requests at once. When the whole grid fits on the GPU
 // in one wave (small batches), a lane with OPW < 8 outputs has registers to
 // keep UPL = 8 / OPW of its (slot, block) units in flight instead of one HBM
@@ -71,9 +83,10 @@ __global__ void __launch_bounds__(kThreads, (OPW * UPL >= 8) ? 2 : 3)
     const float wj = s_w[jj];
     uint32_t a[16];
     ld_act_block(hs + (size_t)jj * (I >> 3), nblk, bb, a);
+    float sc[OPW];
+    unit_scales(U, sc);
 #pragma unroll
-    for (int r = 0; r < OPW; ++r)
-      acc[r] = fmaf(block_dot(a, U.c[r]), e8m0_to_f32(U.s[r]) * wj, acc[r]);
+    for (int r = 0; r < OPW; ++r) acc[r] = fmaf(block_dot(a, U.c[r]), sc[r] * wj, acc[r]);
   };
   // (slot, block) of a unit, advanced by `step` units
   auto advance = [&](int& jj, int& bb, int step) {
@@ -143,11 +156,13 @@ __global__ void __launch_bounds__(kThreads, (OPW * UPL >= 8) ? 2 : 3)
       const float wj = s_w[jj[0]];
       uint32_t a[16];
       ld_act_block(hs + (size_t)jj[0] * (I >> 3), nblk, bb[0], a);
+      float sc[8];
+      unit_scales(U[0], sc);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
 #pragma unroll
         for (int r = 4 * half; r < 4 * half + 4; ++r)
-          if (ok) acc[r] = fmaf(block_dot(a, U[0].c[r]), e8m0_to_f32(U[0].s[r]) * wj, acc[r]);
+          if (ok) acc[r] = fmaf(block_dot(a, U[0].c[r]), sc[r] * wj, acc[r]);
         if (refill) {
           const size_t row0 = (size_t)en * H + o0;
 #pragma unroll

@@ -134,23 +134,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Four E8M0 scales (the bytes of w) -> 2^(s-127) as FP32, through the
-// hardware E8M0 -> BF16x2 conversion (BF16 has E8M0's 8-bit exponent: code 0
-// gives the subnormal 2^-127, code 255 a NaN) and a shift into FP32.
-__device__ __forceinline__ void e8m0x4_to_f32(uint32_t w, float (&f)[4]) {
-  uint32_t r0, r1;
-  asm("{.reg .b16 a, b;\n\t"
-      "mov.b32 {a, b}, %2;\n\t"
-      "cvt.rn.bf16x2.ue8m0x2 %0, a;\n\t"
-      "cvt.rn.bf16x2.ue8m0x2 %1, b;\n\t}"
-      : "=r"(r0), "=r"(r1)
-      : "r"(w));
-  f[0] = __uint_as_float(r0 << 16);
-  f[1] = __uint_as_float(r0 & 0xFFFF0000u);
-  f[2] = __uint_as_float(r1 << 16);
-  f[3] = __uint_as_float(r1 & 0xFFFF0000u);
-}
-
 // The largest exponent field among 8 BF16 values.
 __device__ __forceinline__ uint32_t bf16x8_max_exp(const uint4& v) {
   const uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7F807F80u, v.y & 0x7F807F80u),

@@ -94,8 +94,10 @@ __global__ void __launch_bounds__(kThreads, 3)
       if (FULL || b < nblk) {
         uint32_t a[16];
         ld_act_block(xs, nblk, b, a);
-        acc[s] = fmaf(block_dot(a, U.g[q]), e8m0_to_f32(U.sg[q]), acc[s]);
-        acc[SPW + s] = fmaf(block_dot(a, U.u[q]), e8m0_to_f32(U.su[q]), acc[SPW + s]);
+        float sg, su;
+        e8m0x2_to_f32(U.sg[q], U.su[q], sg, su);
+        acc[s] = fmaf(block_dot(a, U.g[q]), sg, acc[s]);
+        acc[SPW + s] = fmaf(block_dot(a, U.u[q]), su, acc[SPW + s]);
       }
     }
   };

@@ -202,8 +202,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           e4m3x4_to_f16x4(cub[hb].y, a1[1], a1[3]);
           const uint32_t swd = (i % 8) < 4 ? U.sg[i / 8].x : U.sg[i / 8].y;
           const uint32_t uwd = (i % 8) < 4 ? U.su[i / 8].x : U.su[i / 8].y;
-          const float sg = e8m0_to_f32((swd >> (8 * (i % 4))) & 0xFFu);
-          const float su = e8m0_to_f32((uwd >> (8 * (i % 4))) & 0xFFu);
+          float sg, su;
+          e8m0x2_to_f32(swd >> (8 * (i % 4)), uwd >> (8 * (i % 4)), sg, su);
           const int off = hb ? off_odd : off_even;
 #pragma unroll
           for (int c = 0; c < NCH; ++c) {

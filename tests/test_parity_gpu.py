@@ -372,3 +372,58 @@ def test_library_allocates_no_device_memory(tiny):
     free1, _ = torch.cuda.mem_get_info()
     # only torch's caching allocator may have grown (the test's own tensors)
     assert free0 - free1 < 64 << 20
+
+
+def _zero_scale_layer():
+    """A layer (H=256, I=256, E=2, top-1) whose gate row 5 of expert 1 keeps
+    only block 0, with E8M0 scale code 0 (2^-127), and whose down row 7 of
+    expert 1 likewise, in both the oracle's arrays and the device copy."""
+    layer = _rand_layer_shape(256, 256, 2, 1, seed=13)
+    r = layer.ref
+    r.gate_codes[1, 5, 32:] = 0
+    r.gate_scales[1, 5, 0] = 0
+    r.down_codes[1, 7, 32:] = 0
+    r.down_scales[1, 7, 0] = 0
+    H, I = 256, 256
+    gu_c = layer.dev.tensors[0].view(2, I, 2, H)
+    gu_s = layer.dev.tensors[1].view(2, I, 2, H // 32)
+    d_c = layer.dev.tensors[2].view(2, H, I)
+    d_s = layer.dev.tensors[3].view(2, H, I // 32)
+    gu_c[1, 5, 0, 32:] = 0
+    gu_s[1, 5, 0, 0] = 0
+    d_c[1, 7, 32:] = 0
+    d_s[1, 7, 0] = 0
+    return layer
+
+
+@pytest.mark.parametrize("down_form", ["per_token", "grouped"])
+def test_scale_code_zero_decodes_to_two_to_the_minus_127(down_form):
+    """E8M0 code 0 is 2^-127, not 0 (the kernels decode scales with the
+    hardware E8M0 -> BF16 conversion). Activations of about 2^110 make the
+    one remaining block of gate row 5 give a visible g, and an intermediate of
+    about 2^100 makes down row 7's block give a visible y; both rows would
+    read 0 if code 0 decoded to 0."""
+    layer = _zero_scale_layer()
+    xf = workload.bf16_bits_to_f32(workload.tokens(layer.shape, 1, seed=3)[0]).astype(np.float64)
+    xb = torch.from_numpy((xf * 2.0**110).astype(np.float32)).to(torch.bfloat16)
+    x = xb.view(torch.int16).numpy().view(np.uint16)
+    ids = np.array([[1]], np.int32)
+    w = np.ones((1, 1), np.float32)
+    _, h = _run_layer(layer, x, ids, w)
+    y_ref, h_ref, _ = oracle.moe_layer(layer.ref, x, ids, w, return_h=True)
+    assert _bf16_vals(h_ref[0, 0, 5:6])[0] != 0.0
+    _check_h(h, h_ref)
+    # down alone, from an intermediate of about 2^100
+    hb = torch.from_numpy((np.linspace(-1, 1, 256) * 2.0**100).astype(np.float32)).to(torch.bfloat16)
+    hbits = hb.view(torch.int16).numpy().view(np.uint16).reshape(1, 1, 256)
+    y = torch.empty((1, 256), dtype=torch.float32, device="cuda")
+    fn = ops.moe_down if down_form == "per_token" else ops.moe_down_grouped
+    fn(layer.dev, _dev(hbits.view(np.int16)), _dev(ids), _dev(w), y)
+    torch.cuda.synchronize()
+    wd = oracle.dequantize_mxfp8(layer.ref.down_codes[1], layer.ref.down_scales[1])  # [H, I]
+    y_exp = wd @ _bf16_vals(hbits[0, 0])
+    yg = y.cpu().numpy()[0].astype(np.float64)
+    assert y_exp[7] != 0.0
+    rel = np.abs(yg - y_exp) / np.maximum(np.abs(y_exp), 1e-30 * 2.0**100)
+    assert rel[7] <= 1e-5, (yg[7], y_exp[7])
+    assert np.max(np.abs(yg - y_exp)) <= 1e-5 * np.max(np.abs(y_exp))
