@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--down-forms", action="store_true",
                     help="with --sweep: also time moe_down and moe_down_grouped alone "
                          "(CUDA graph, same rotation) for every workload")
+    ap.add_argument("--kernels-once", metavar="WORKLOAD", default=None,
+                    help="for ncu: build layer 0 of WORKLOAD, then launch every gate/up and "
+                         "down kernel twice on its first batch (eager), and exit")
     ap.add_argument("--sweep", nargs="*", default=None,
                     help="instead of the single contract line, print one line per workload "
                          "(default: the batch sweep of the pages' metric), timing CUDA-graph "
@@ -104,6 +107,7 @@ KERNEL_SOURCES = {
     "moe_gate_up": ["wd_device.cuh", "wd_gate_up.cuh", "wd_gate_up.cu", "wd_gate_up_fixed.cu"],
     "moe_gate_up_grouped": ["wd_device.cuh", "wd_gate_up_grouped.h", "wd_gate_up_grouped.cu"],
     "moe_down": ["wd_device.cuh", "wd_down.cu"],
+    "moe_down_grouped": ["wd_device.cuh", "wd_down_grouped.h", "wd_down_grouped.cu"],
 }
 
 
@@ -127,7 +131,7 @@ def ncu_traffic(kernel: str, workload: str):
     ent = d.get(kernel, {}).get(workload)
     if not ent or ent.get("kernel_sha") != kernel_source_sha(kernel):
         return None
-    return ent.get("dram_bytes_per_launch")
+    return ent.get("dram_bytes_per_launch"), ent.get("algorithmic_bytes_same_launches")
 
 
 # ------------------------------------------------------------ multi-rank --
@@ -513,7 +517,7 @@ def run_ours(args, wl, rank, world, local_rank):
     sweep = acc = None
     if not args.no_sweep:
         sweep, acc = metric_sweep(layers, dev, peak)
-    traffic = ncu_traffic(gu_kernel, wl.name)
+    traffic, traffic_alg = ncu_traffic(gu_kernel, wl.name) or (None, None)
     gu_launch_bytes = sum(gu_bytes) / args.steps
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -537,7 +541,10 @@ def run_ours(args, wl, rank, world, local_rank):
         "roofline": {"bound": "hbm", "kernel": gu_kernel, "achieved": gu_gbs, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": gu_gbs / peak,
                      "algorithmic_bytes_per_launch": gu_launch_bytes,
-                     "traffic": traffic},
+                     "traffic": traffic,
+                     "traffic_note": None if traffic is None else
+                     f"mean of the ncu-captured launches, whose own algorithmic bytes average "
+                     f"{traffic_alg} (ratio {traffic / traffic_alg:.4f}); profiles/traffic.json"},
         "cpu_baseline": cpu,
         "cpu_baseline_all_cores": cpu_all,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -834,8 +841,45 @@ def run_sweep(names, steps: int, gate_up_forms: bool = False, down_forms: bool =
               flush=True)
 
 
+def run_kernels_once(name: str):
+    """Each kernel of the layer, launched twice on the first token batch of a
+    workload (layer 0 of the bench's weights): moe_gate_up, moe_gate_up_grouped,
+    moe_down, moe_down_grouped (the grouped ones where they take the shape and
+    batch). A target for ncu captures of one kernel (-k regex:<name> -s 1 -c 1)."""
+    import torch
+
+    from output_centric_expert_gb300 import ops, workload
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = workload.WORKLOADS[name]
+    s = wl.shape
+    L = build_device_layers(s, 1, 0, dev)[0]
+    x, ids, w = make_batches(wl, 1, 0)[0]
+    xd = torch.from_numpy(x.view(np.int16)).to(dev)
+    idd = torch.from_numpy(ids).to(dev)
+    wd = torch.from_numpy(w).to(dev)
+    h = torch.empty((wl.B, s.top_k, s.I), dtype=torch.int16, device=dev)
+    y = torch.empty((wl.B, s.H), dtype=torch.float32, device=dev)
+    ran = []
+    for kname, fn, args in (("moe_gate_up", ops.moe_gate_up, (L, xd, idd, h)),
+                            ("moe_gate_up_grouped", ops.moe_gate_up_grouped, (L, xd, idd, h)),
+                            ("moe_down", ops.moe_down, (L, h, idd, wd, y)),
+                            ("moe_down_grouped", ops.moe_down_grouped, (L, h, idd, wd, y))):
+        try:
+            for _ in range(2):
+                fn(*args)
+            ran.append(kname)
+        except ops.WarpDecodeError:
+            pass
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"kernels_once": name, "launched_twice": ran}), flush=True)
+
+
 def main():
     args = parse()
+    if args.kernels_once is not None:
+        run_kernels_once(args.kernels_once)
+        return
     if args.sweep is not None:
         run_sweep(args.sweep or SWEEP_DEFAULT, args.steps, args.gate_up_forms, args.down_forms)
         return
