@@ -29,8 +29,9 @@
  * consecutive elements along the reduction axis (H for gate/up, I for down).
  *
  * Conventions for every entry point:
- *  - Shapes: H % 32 == 0 and H <= 8192, I % 32 == 0, E >= 1,
- *    1 <= top_k <= E, B >= 0.
+ *  - Shapes: H % 32 == 0 and H <= 8192, I % 32 == 0, E >= 1, top_k >= 1
+ *    (ids may repeat, so top_k may exceed E, e.g. on a shard of the experts;
+ *    routing from logits needs top_k <= E), B >= 0.
  *    B == 0 is a valid empty batch: nothing is launched, MOE_OK is returned.
  *  - Device pointers: caller-owned (e.g. torch allocations). The two code
  *    arrays (gu_codes, d_codes) must be 32-byte aligned, x and h 16-byte
@@ -244,7 +245,7 @@ moe_status moe_layer_host(const moe_shape* shape, const moe_weights* w, const ui
  *   wts    [B][top_k] FP32, written: exp(l_j - l_max) / sum over the chosen i
  *                     of exp(l_i - l_max) (= the softmax renormalised over the
  *                     chosen experts)
- * Needs E <= 256 and top_k <= 32 (MOE_ERR_UNSUPPORTED otherwise).
+ * Needs E <= 256 and top_k <= min(32, E) (MOE_ERR_UNSUPPORTED otherwise).
  */
 moe_status moe_route(const moe_shape* shape, const float* logits, int32_t B, int32_t* ids,
                      float* wts, void* stream);
@@ -294,6 +295,24 @@ moe_status moe_layer_routed(const moe_shape* shape, const moe_weights* w, const 
 moe_status moe_layer_noalloc(const moe_shape* shape, const moe_weights* w, const uint16_t* x,
                              const int32_t* ids, const float* wts, int32_t B, float* y,
                              int32_t* err_flag, void* stream);
+
+/*
+ * moe_local_ids -- expert parallelism (the layer split over G devices, each
+ * holding a contiguous range of experts; y is then the sum of the devices'
+ * results, one all-reduce). The slots of a batch that the shard holding
+ * experts [e_first, e_first + e_count) computes:
+ *   local_ids[t,j] = ids[t,j] - e_first  if e_first <= ids[t,j] < e_first + e_count
+ *                    -1                  otherwise (contributes nothing on this shard)
+ * A shard then runs the layer on its own experts (shape with E = e_count) with
+ * local_ids and a NULL err_flag; ids outside [0, shape->E) (the global E) set
+ * bit 0 of *err_flag here instead, if err_flag is non-NULL. ids and local_ids
+ * [B][top_k] int32, device, 4-byte aligned. Requires 0 <= e_first and
+ * 1 <= e_count <= shape->E - e_first (MOE_ERR_SHAPE otherwise). The pages
+ * describe no multi-device split; this is the one the expert-major weight
+ * layout allows with a single exchange.
+ */
+moe_status moe_local_ids(const moe_shape* shape, const int32_t* ids, int32_t B, int32_t e_first,
+                         int32_t e_count, int32_t* local_ids, int32_t* err_flag, void* stream);
 
 /* Static description of a status code. */
 const char* moe_status_string(moe_status status);

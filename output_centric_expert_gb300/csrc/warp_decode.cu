@@ -37,6 +37,17 @@ int sm_count() {
 
 namespace {
 
+// moe_local_ids: one thread per (token, slot).
+__global__ void __launch_bounds__(kThreads)
+    moe_local_ids_kernel(const int32_t* __restrict__ ids, int32_t* __restrict__ local, int P,
+                         int E, int e_first, int e_count, int32_t* __restrict__ err) {
+  const int p = blockIdx.x * kThreads + threadIdx.x;
+  if (p >= P) return;
+  const int e = __ldg(ids + p);
+  if (e < 0 || e >= E) flag_invalid(err);
+  local[p] = (e >= e_first && e < e_first + e_count) ? e - e_first : -1;
+}
+
 // moe_route: one warp per token.
 __global__ void __launch_bounds__(kThreads)
     moe_route_kernel(const float* __restrict__ logits, int32_t* __restrict__ ids,
@@ -56,9 +67,8 @@ __global__ void __launch_bounds__(kThreads)
 
 moe_status check_shape(const moe_shape* s, int32_t B) {
   if (!s) return MOE_ERR_NULL;
-  if (s->H <= 0 || s->I <= 0 || s->E <= 0 || s->top_k <= 0 || s->top_k > s->E || B < 0 ||
-      s->H % 32 || s->I % 32) {
-    set_error_msg("shape: need H%32==0, I%32==0, E>=1, 1<=top_k<=E, B>=0");
+  if (s->H <= 0 || s->I <= 0 || s->E <= 0 || s->top_k <= 0 || B < 0 || s->H % 32 || s->I % 32) {
+    set_error_msg("shape: need H%32==0, I%32==0, E>=1, top_k>=1, B>=0");
     return MOE_ERR_SHAPE;
   }
   if (s->H > 8192) {
@@ -95,11 +105,12 @@ moe_status launch_status(const char* what) {
 }
 
 // Checks of the routed entry points: the warp router handles E <= 256 and
-// top_k <= 32; logits are FP32 [B][E], 4-byte aligned.
+// top_k <= 32 distinct choices (top_k <= E); logits are FP32 [B][E], 4-byte
+// aligned.
 moe_status check_route(const moe_shape* s, const float* logits) {
   if (!logits) return MOE_ERR_NULL;
-  if (s->E > kRouteMaxE || s->top_k > 32) {
-    set_error_msg("routing on the device needs E <= 256 and top_k <= 32");
+  if (s->E > kRouteMaxE || s->top_k > 32 || s->top_k > s->E) {
+    set_error_msg("routing on the device needs E <= 256 and top_k <= min(32, E)");
     return MOE_ERR_UNSUPPORTED;
   }
   if (!aligned(logits, 4)) {
@@ -358,6 +369,29 @@ extern "C" moe_status moe_layer_host(const moe_shape* shape, const moe_weights* 
     return MOE_ERR_CUDA;
   }
   return MOE_OK;
+}
+
+extern "C" moe_status moe_local_ids(const moe_shape* shape, const int32_t* ids, int32_t B,
+                                    int32_t e_first, int32_t e_count, int32_t* local_ids,
+                                    int32_t* err_flag, void* stream) {
+  using namespace wd;
+  moe_status rc = check_shape(shape, B);
+  if (rc != MOE_OK) return rc;
+  if (e_first < 0 || e_count < 1 || e_count > shape->E - e_first) {
+    set_error_msg("moe_local_ids: need 0 <= e_first and 1 <= e_count <= E - e_first");
+    return MOE_ERR_SHAPE;
+  }
+  if (B == 0) return MOE_OK;
+  if (!ids || !local_ids) return MOE_ERR_NULL;
+  if (!aligned(ids, 4) || !aligned(local_ids, 4) || !aligned(err_flag, 4)) {
+    set_error_msg("alignment: ids, local_ids and err_flag need 4 bytes");
+    return MOE_ERR_ALIGN;
+  }
+  const int64_t P = (int64_t)B * shape->top_k;
+  const unsigned grid = (unsigned)((P + kThreads - 1) / kThreads);
+  moe_local_ids_kernel<<<grid, kThreads, 0, (cudaStream_t)stream>>>(
+      ids, local_ids, (int)P, shape->E, e_first, e_count, err_flag);
+  return launch_status("moe_local_ids launch");
 }
 
 extern "C" const char* moe_status_string(moe_status s) {

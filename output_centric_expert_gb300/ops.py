@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.moe_layer_noalloc.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp]
         L.moe_layer_host.restype = ctypes.c_int
         L.moe_layer_host.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.moe_local_ids.restype = ctypes.c_int
+        L.moe_local_ids.argtypes = [sp, vp, i32, i32, i32, vp, vp, vp]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_status_string.argtypes = [ctypes.c_int]
         L.moe_last_error.restype = ctypes.c_char_p
@@ -324,10 +326,22 @@ def moe_layer_host(weights: DeviceWeights, x_host: torch.Tensor, ids_host: torch
     return y_host
 
 
+def moe_local_ids(shape: MoeShape, ids: torch.Tensor, e_first: int, e_count: int,
+                  local_ids: torch.Tensor, err_flag: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """local_ids[t,j] = ids[t,j] - e_first for the shard's experts, else -1."""
+    B = ids.shape[0]
+    _check("moe_local_ids", lib().moe_local_ids(
+        ctypes.byref(shape), _ptr(ids, (torch.int32,), "ids"), B, e_first, e_count,
+        _ptr(local_ids, (torch.int32,), "local_ids"), _ptr(err_flag, (torch.int32,), "err_flag"),
+        _stream(stream)))
+    return local_ids
+
+
 def exported_symbols() -> list[str]:
     """The entry points include/warp_decode.h declares."""
     return ["moe_packed_bytes", "moe_pack_weights", "moe_gate_up", "moe_gate_up_grouped",
             "moe_layer_gate_up_kernel", "moe_down", "moe_down_grouped",
             "moe_layer_down_kernel", "moe_layer",
             "moe_layer_host", "moe_layer_noalloc", "moe_route", "moe_layer_routed",
-            "moe_status_string", "moe_last_error"]
+            "moe_local_ids", "moe_status_string", "moe_last_error"]

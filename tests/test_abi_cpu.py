@@ -47,9 +47,13 @@ def test_host_validation_rejects_before_launch():
     assert gate_up(None, w, P, P, 1, P) == 1  # MOE_ERR_NULL
     assert gate_up(sh, None, P, P, 1, P) == 1
     assert gate_up(sh, w, None, P, 1, P) == 1
-    for bad in ((250, 128, 8, 2), (256, 100, 8, 2), (256, 128, 0, 1), (256, 128, 8, 9), (256, 128, 8, 0),
+    for bad in ((250, 128, 8, 2), (256, 100, 8, 2), (256, 128, 0, 1), (256, 128, 8, 0),
                 (8224, 128, 8, 2)):
         assert gate_up(ops.make_shape(*bad), w, P, P, 1, P) == 2  # MOE_ERR_SHAPE
+    # top_k may exceed E (ids repeat; an expert-parallel shard holds fewer experts
+    # than top_k), but routing from logits needs top_k distinct experts
+    assert gate_up(ops.make_shape(256, 128, 8, 9), w, None, None, 0, None) == 0
+    assert L.moe_route(ctypes.byref(ops.make_shape(256, 128, 8, 9)), P, 1, P, P, None) == 5
     assert gate_up(sh, w, P, P, -1, P) == 2
     assert gate_up(sh, _fake_weights(aligned=False), P, P, 1, P) == 3  # MOE_ERR_ALIGN
     assert gate_up(sh, w, P + 2, P, 1, P) == 3
@@ -142,7 +146,8 @@ static const any_fn entry_points[] = {
   (any_fn)moe_packed_bytes, (any_fn)moe_pack_weights, (any_fn)moe_gate_up,
   (any_fn)moe_gate_up_grouped, (any_fn)moe_layer_gate_up_kernel, (any_fn)moe_down,
   (any_fn)moe_down_grouped, (any_fn)moe_layer_down_kernel, (any_fn)moe_layer, (any_fn)moe_layer_host, (any_fn)moe_route, (any_fn)moe_layer_routed,
-  (any_fn)moe_layer_noalloc, (any_fn)moe_status_string, (any_fn)moe_last_error,
+  (any_fn)moe_layer_noalloc, (any_fn)moe_local_ids, (any_fn)moe_status_string,
+  (any_fn)moe_last_error,
 };
 
 int main(void) {

@@ -235,3 +235,59 @@ def test_grouped_down_refuses_what_it_cannot_take(q30):
                              ids, torch.zeros((B, 8), dtype=torch.float32, device="cuda"),
                              torch.zeros((B, 2048), dtype=torch.float32, device="cuda"))
     assert ei.value.status == 5
+
+
+@pytest.mark.parametrize("world,B", [(2, 32), (3, 64), (32, 8)])
+def test_expert_parallel_shards_sum_to_the_layer(q30, world, B):
+    """The layer split over `world` expert shards on one device, one shard at a
+    time (moe_local_ids, then moe_layer on the shard's experts with no error
+    flag), summed on the host: within the parity bar of the whole layer and of
+    the oracle. 32 shards hold 4 experts each, fewer than top_k."""
+    from output_centric_expert_gb300 import expert_parallel as ep
+    s = q30.shape
+    x, ids, w = workload.tokens(s, B, batch=900 + B)
+    xd, idd, wd = _dev(x.view(np.int16)), _dev(ids), _dev(w)
+    total = torch.zeros((B, s.H), dtype=torch.float64, device="cuda")
+    local = torch.empty_like(idd)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    covered = 0
+    for r in range(world):
+        first, count = ep.shard_range(s.E, r, world)
+        part = ep.shard_packed(q30.packed, s, first, count)
+        shard = ops.DeviceWeights(ops.make_shape(s.H, s.I, count, s.top_k), part)
+        h = torch.empty((B, s.top_k, s.I), dtype=torch.int16, device="cuda")
+        y = torch.empty((B, s.H), dtype=torch.float32, device="cuda")
+        ep.ep_layer(shard, xd, idd, wd, h, y, first, count, global_E=s.E, local_ids=local,
+                    err_flag=err, all_reduce=False)
+        torch.cuda.synchronize()
+        lid = local.cpu().numpy()
+        want = np.where((ids >= first) & (ids < first + count), ids - first, -1)
+        assert np.array_equal(lid, want)
+        covered += int((lid >= 0).sum())
+        total += y.double()
+    assert covered == B * s.top_k and int(err.item()) == 0
+    h = torch.empty((B, s.top_k, s.I), dtype=torch.int16, device="cuda")
+    y_all = torch.empty((B, s.H), dtype=torch.float32, device="cuda")
+    ops.moe_layer(q30.dev, xd, idd, wd, h, y_all)
+    torch.cuda.synchronize()
+    # a shard has fewer experts, so the layer may choose the other gate/up
+    # kernel for it than for the whole layer (an intermediate can then differ
+    # by one BF16 step): the layer's parity bar applies
+    d, cos = parity_stats(total.cpu().numpy(), y_all.cpu().numpy().astype(np.float64))
+    assert d <= MAX_ABS and cos >= MIN_COS, (d, cos)
+    sample = [0, B - 1]
+    y_ref, _ = oracle.moe_layer(q30.ref, x[sample], ids[sample], w[sample])
+    _check_y(total.cpu().numpy()[sample], y_ref)
+
+
+def test_local_ids_flag_ids_outside_the_global_range(q30):
+    ids = torch.tensor([[0, 5, 127, 128], [-1, 64, 63, 3]], dtype=torch.int32, device="cuda")
+    local = torch.empty_like(ids)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sh = ops.make_shape(2048, 768, 128, 4)
+    ops.moe_local_ids(sh, ids, 64, 64, local, err)
+    torch.cuda.synchronize()
+    assert local.cpu().tolist() == [[-1, -1, 63, -1], [-1, 0, -1, -1]]
+    assert int(err.item()) == 1
+    with pytest.raises(ops.WarpDecodeError):
+        ops.moe_local_ids(sh, ids, 64, 65, local)
