@@ -103,11 +103,24 @@ def study(B=8, batch=321):
     return out
 
 
+# token batches of the study: (tokens, batch index of the seeded generator)
+STUDY_BATCHES = ((8, 321), (4, 322), (4, 323), (4, 324))
+PAGES_RATIO = 1.4  # [§Improved accuracy]: 1.4x closer to the FP32 reference
+
+
 def test_warp_decode_is_closer_than_the_activation_round_trip():
-    res = study()
-    print(res)
-    # the direction the pages report, under both readings of the reference
-    assert res["same MXFP8 weights"]["ratio"] > 1.0
-    # against the unquantised FP32 weights the pages' factor, 1.4x closer
-    # ([§Improved accuracy]), is reproduced on these synthetic inputs
-    assert 1.25 < res["FP32 weights"]["ratio"] < 1.6
+    """Four independent token batches (20 tokens, about 110 experts): on every
+    batch warp decode is closer to both references than the activation round
+    trip, and against the unquantised FP32 weights the mean factor lies within
+    15 % of the pages' 1.4; the per-batch spread is printed."""
+    ratios = []
+    for B, batch in STUDY_BATCHES:
+        res = study(B, batch)
+        print(B, batch, {k: round(v["ratio"], 3) for k, v in res.items()})
+        # the direction the pages report, under both readings of the reference
+        assert res["same MXFP8 weights"]["ratio"] > 1.0
+        assert res["FP32 weights"]["ratio"] > 1.0
+        ratios.append(res["FP32 weights"]["ratio"])
+    mean = float(np.mean(ratios))
+    print("FP32-weights ratio per batch", [round(r, 3) for r in ratios], "mean", round(mean, 3))
+    assert abs(mean - PAGES_RATIO) <= 0.15 * PAGES_RATIO
