@@ -133,7 +133,8 @@ moe_status moe_gate_up(const moe_shape* shape, const moe_weights* w, const uint1
  * result as for moe_gate_up; the sums differ from moe_gate_up's only in
  * FP32 rounding order; a pair's result does not depend on the other pairs
  * of the batch. Returns MOE_ERR_UNSUPPORTED, launching nothing, unless
- * H % 256 == 0, I % 64 == 0 and gu_scales is 8-byte aligned.
+ * H % 256 == 0, I % 64 == 0, E <= 256, gu_scales is 8-byte aligned and the
+ * batch's pair lists fit in one CTA's shared memory.
  * moe_layer and the other layer entry points use this kernel by themselves
  * when 2 * B * top_k >= 5 * E and the shape allows it (measured faster there
  * on GB300: each weight is decoded once instead of once per pair); below

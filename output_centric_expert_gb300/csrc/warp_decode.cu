@@ -131,9 +131,9 @@ moe_status gate_up_impl(const moe_shape* s, const moe_weights* w, const uint16_t
   moe_status rc = check_shape(s, B);
   if (rc != MOE_OK) return rc;
   if ((rc = check_weights(w, true, false)) != MOE_OK) return rc;
-  if (form == GateUpForm::kGrouped && !gate_up_grouped_supported(s, w)) {
-    set_error_msg("moe_gate_up_grouped: needs H % 256 == 0, I % 64 == 0 and 8-byte aligned "
-                  "gu_scales");
+  if (form == GateUpForm::kGrouped && !gate_up_grouped_supported(s, w, B)) {
+    set_error_msg("moe_gate_up_grouped: needs H % 256 == 0, I % 64 == 0, E <= 256, 8-byte "
+                  "aligned gu_scales and the batch's tables within shared memory");
     return MOE_ERR_UNSUPPORTED;
   }
   if (B == 0) return MOE_OK;
@@ -157,7 +157,7 @@ moe_status gate_up_impl(const moe_shape* s, const moe_weights* w, const uint16_t
 // the Qwen-3-235B-A22B shape (1.06 E): each weight is decoded once rather
 // than once per routed pair.
 GateUpForm layer_form(const moe_shape* s, const moe_weights* w, int32_t B) {
-  if (s && 2 * (int64_t)B * s->top_k >= 5 * (int64_t)s->E && gate_up_grouped_supported(s, w))
+  if (s && 2 * (int64_t)B * s->top_k >= 5 * (int64_t)s->E && gate_up_grouped_supported(s, w, B))
     return GateUpForm::kGrouped;
   return GateUpForm::kPerToken;
 }

@@ -8,10 +8,10 @@
 
 namespace wd {
 
-// Whether the grouped kernel handles the shape and weights: H % 256 == 0,
-// I % 64 == 0, gu_scales 8-byte aligned (not checked when w is NULL), and the
-// grid within CUDA's limit.
-bool gate_up_grouped_supported(const moe_shape* s, const moe_weights* w);
+// Whether the grouped kernel handles the shape, batch and weights:
+// H % 256 == 0, I % 64 == 0, E <= 256, gu_scales 8-byte aligned (not checked
+// when w is NULL), and its shared memory for B tokens within the limit.
+bool gate_up_grouped_supported(const moe_shape* s, const moe_weights* w, int32_t B);
 
 // Launch it on `st` (expert ids only, no routing from logits); the arguments
 // have been validated by the entry point. Returns MOE_OK or an error status.

@@ -122,9 +122,9 @@ def test_grouped_small_shapes(H, I, E, k, B):
     _check_h(h, h_ref)
 
 
-@pytest.mark.parametrize("H,I", [(96, 160), (2080, 800), (2048, 96)])
-def test_grouped_refuses_unsupported_shapes(H, I):
-    layer = Layer(workload.LayerShape(H, I, 2, 1), seed=1)
+@pytest.mark.parametrize("H,I,E", [(96, 160, 2), (2080, 800, 2), (2048, 96, 2), (256, 64, 257)])
+def test_grouped_refuses_unsupported_shapes(H, I, E):
+    layer = Layer(workload.LayerShape(H, I, E, 1), seed=1)
     x, ids, _ = workload.tokens(layer.shape, 1, seed=3)
     with pytest.raises(ops.WarpDecodeError) as exc:
         _grouped(layer, x, ids)
