@@ -15,11 +15,21 @@
  *                 streamed over all top-k experts' down rows with the routing
  *                 weight folded in, then reduced across the 32 lanes by a
  *                 butterfly shuffle. No per-expert output buffer exists.
- * For batches where many routed pairs share each expert (2 * B * top_k >=
- * 5 * E), the layer computes the gate/up step with an expert-grouped kernel
- * instead (moe_gate_up_grouped: one warp per (expert, 8 neurons) for all the
- * pairs routed to that expert, multiplying on tensor cores); each
- * intermediate is still written once by one warp, with the same numerics.
+ * For batches where many routed pairs share each expert (see
+ * LAYER KERNEL CHOICE below), the layer computes each step with an
+ * expert-grouped kernel instead (moe_gate_up_grouped: one warp per (expert,
+ * 8 neurons) for all the pairs routed to that expert; moe_down_grouped: one
+ * CTA per 16 output rows for every token), multiplying on tensor cores and
+ * decoding each weight once; each output is still written once, with the
+ * same numerics up to FP32 rounding order.
+ *
+ * LAYER KERNEL CHOICE (moe_layer, moe_layer_host, moe_layer_noalloc,
+ * moe_layer_routed with ids_out), with P = B * top_k routed pairs, measured
+ * on GB300 under uniform routing:
+ *   gate/up grouped when 2P >= 5E (H < 4096), 2P >= 3E (H >= 4096);
+ *   down grouped when    2P >= 5E (H < 6144), P >= 2E (H >= 6144);
+ * each only where the grouped kernel takes the shape and batch. The choice
+ * is reported by moe_layer_gate_up_kernel and moe_layer_down_kernel.
  *
  * Numerics (fixed by this API):
  *   g = sum_h x[t,h] Wg[e,n,h],  u = sum_h x[t,h] Wu[e,n,h]     (FP32 accum.)
@@ -136,11 +146,11 @@ moe_status moe_gate_up(const moe_shape* shape, const moe_weights* w, const uint1
  * H % 256 == 0, I % 64 == 0, E <= 256, gu_scales is 8-byte aligned and the
  * batch's pair lists fit in one CTA's shared memory.
  * moe_layer and the other layer entry points use this kernel by themselves
- * when 2 * B * top_k >= 5 * E and the shape allows it (measured faster there
- * on GB300: each weight is decoded once instead of once per pair); below
- * that, and when routing from logits without ids_out, they use moe_gate_up's
+ * where the LAYER KERNEL CHOICE above says so (measured faster there on
+ * GB300: each weight is decoded once instead of once per pair); elsewhere,
+ * and when routing from logits without ids_out, they use moe_gate_up's
  * kernel. The two kernels agree to FP32 rounding order, so a token's result
- * can change in its last bits when the batch crosses that size.
+ * can change in its last bits when the batch crosses the switch.
  */
 moe_status moe_gate_up_grouped(const moe_shape* shape, const moe_weights* w,
                                const uint16_t* x, const int32_t* ids, int32_t B, uint16_t* h,
@@ -191,9 +201,8 @@ moe_status moe_down(const moe_shape* shape, const moe_weights* w, const uint16_t
  * on every call with the same inputs. Returns MOE_ERR_UNSUPPORTED, launching
  * nothing, unless I % 256 == 0, E <= 256, 1 <= B <= 128 (B == 0 is an empty
  * batch), d_scales is 8-byte aligned and the batch's tables fit in one CTA's
- * shared memory. The layer entry points use this kernel by themselves when
- * B * top_k >= 3 * E and it takes the shape and batch (measured faster there
- * on GB300; see moe_layer_down_kernel).
+ * shared memory. The layer entry points use this kernel by themselves where
+ * the LAYER KERNEL CHOICE above says so and it takes the shape and batch.
  */
 moe_status moe_down_grouped(const moe_shape* shape, const moe_weights* w, const uint16_t* h,
                             const int32_t* ids, const float* wts, int32_t B, float* y,
@@ -212,8 +221,8 @@ moe_status moe_layer_down_kernel(const moe_shape* shape, const moe_weights* w, i
 
 /*
  * moe_layer -- the whole layer: the gate/up step then moe_down on `stream`.
- * The gate/up step runs moe_gate_up's kernel, or moe_gate_up_grouped's when
- * 2 * B * top_k >= 5 * E and that kernel takes the shape (see there).
+ * Each step runs its per-token or its expert-grouped kernel as the LAYER
+ * KERNEL CHOICE above says.
  * h_scratch [B][top_k][I] BF16 is caller-provided device memory that holds
  * the intermediate between the two kernels (its contents afterwards are the
  * intermediate, as from the gate/up kernel that ran).
@@ -253,8 +262,8 @@ moe_status moe_route(const moe_shape* shape, const float* logits, int32_t B, int
 
 /*
  * moe_layer_routed -- the layer from router logits (the same choice as
- * moe_route). Two ways, with the same results bit for bit below
- * 2 * B * top_k = 5 * E:
+ * moe_route). Two ways, with the same results bit for bit where the layer
+ * runs the per-token kernels (LAYER KERNEL CHOICE above):
  *  - ids_out and wts_out both non-NULL ([B][top_k], as moe_route): every token
  *    is routed once into them by the router kernel, and the layer reads that
  *    routing exactly as moe_layer does (same choice of gate/up kernel). The
@@ -262,8 +271,8 @@ moe_status moe_route(const moe_shape* shape, const float* logits, int32_t B, int
  *  - both NULL: no ids/weights array exists at all. Every warp of moe_gate_up
  *    and moe_down routes its token from `logits` itself before it requests
  *    weights, which costs about 30 % of the layer at B=32. This way always
- *    uses moe_gate_up's per-token kernel, so from 2 * B * top_k >= 5 * E it
- *    agrees with the other way to FP32 rounding order, not bit for bit.
+ *    uses the per-token kernels, so where the layer would run a grouped one
+ *    it agrees with the other way to FP32 rounding order, not bit for bit.
  * Same limits as moe_route; other arguments as for moe_layer.
  */
 moe_status moe_layer_routed(const moe_shape* shape, const moe_weights* w, const uint16_t* x,

@@ -151,14 +151,22 @@ moe_status gate_up_impl(const moe_shape* s, const moe_weights* w, const uint16_t
 }
 
 // The form of moe_gate_up a layer entry point uses: the expert-grouped kernel
-// once B * top_k >= 2.5 * E, if the shape allows it. Measured on GB300 under
-// uniform routing, the grouped kernel overtakes the per-token one at about
-// 36 tokens for the Qwen-3-30B-A3B shape (2.25 E pairs) and 17 tokens for
-// the Qwen-3-235B-A22B shape (1.06 E): each weight is decoded once rather
-// than once per routed pair.
+// once the batch has enough pairs per expert, if the shape allows it. The
+// switch points are measured on GB300 (each kernel alone, CUDA graph, cold
+// L2, uniform routing): per-token vs grouped gate/up break even at about 36
+// tokens for the Qwen-3-30B-A3B shape (2.25 E pairs; H = 2048), 19 for the
+// Qwen-3-235B-A22B shape (1.2 E; H = 4096), 5 for the Mixtral shape (1.25 E;
+// H = 4096) and 46 for the DeepSeek-V3 shape (1.45 E; H = 7168). The longer
+// rows make each (token, expert) pair dearer for the per-token kernel. Inside
+// the layer the grouped kernel overlaps less with moe_down, so the switch is
+// set a little later (Qwen-3-235B-A22B layer at 20 tokens: 330.5 us per-token
+// vs 339.3 grouped; at 24: 376.5 vs 370.0).
 GateUpForm layer_form(const moe_shape* s, const moe_weights* w, int32_t B) {
-  if (s && 2 * (int64_t)B * s->top_k >= 5 * (int64_t)s->E && gate_up_grouped_supported(s, w, B))
-    return GateUpForm::kGrouped;
+  if (!s) return GateUpForm::kPerToken;
+  const int64_t pairs = (int64_t)B * s->top_k, E = s->E;
+  const bool shared = s->H >= 4096 ? 2 * pairs >= 3 * E   // 1.5 E pairs
+                                   : 2 * pairs >= 5 * E;  // 2.5 E
+  if (shared && gate_up_grouped_supported(s, w, B)) return GateUpForm::kGrouped;
   return GateUpForm::kPerToken;
 }
 
@@ -194,14 +202,17 @@ moe_status down_impl(const moe_shape* s, const moe_weights* w, const uint16_t* h
 }
 
 // The form of moe_down a layer entry point uses: the expert-grouped kernel once
-// B * top_k >= 3 * E, if it takes the shape and batch. Measured on GB300 (each
-// kernel alone, CUDA graph, cold L2), per-token vs grouped: Qwen-3-30B-A3B
-// shape 43.1 vs 46.4 us at 32 tokens (2 pairs per expert), 74.1 vs 66.3 at 64;
-// Qwen-3-235B-A22B shape 99.5 vs 117.4 at 16, 306.1 vs 241.8 at 64;
-// Mixtral-shaped (4 pairs per expert at 16 tokens) 210.0 vs 188.6.
+// the batch has enough pairs per expert, if it takes the shape and batch.
+// Measured on GB300 (each kernel alone, CUDA graph, cold L2, uniform
+// routing), per-token vs grouped down break even at about 37 tokens for the
+// Qwen-3-30B-A3B shape (43.8 vs 46.4 us at 32, 52.2 vs 50.7 at 40), 33 for
+// the Qwen-3-235B-A22B shape, 8 for the Mixtral shape (2 E pairs) and 55 for
+// the DeepSeek-V3 shape (1.7 E).
 DownForm layer_down_form(const moe_shape* s, const moe_weights* w, int32_t B) {
-  if (s && (int64_t)B * s->top_k >= 3 * (int64_t)s->E && down_grouped_supported(s, w, B))
-    return DownForm::kGrouped;
+  if (!s) return DownForm::kPerToken;
+  const int64_t pairs = (int64_t)B * s->top_k, E = s->E;
+  const bool shared = s->H >= 6144 ? pairs >= 2 * E : 2 * pairs >= 5 * E;
+  if (shared && down_grouped_supported(s, w, B)) return DownForm::kGrouped;
   return DownForm::kPerToken;
 }
 

@@ -91,6 +91,12 @@ WORKLOADS: dict[str, Workload] = {
     **{f"q235_b{b}": Workload(f"q235_b{b}", SHAPES["q235"], b) for b in (1, 16, 64)},
     **{f"dsv3_b{b}": Workload(f"dsv3_b{b}", SHAPES["dsv3"], b) for b in (1, 16, 64)},
     **{f"mixtral_b{b}": Workload(f"mixtral_b{b}", SHAPES["mixtral"], b) for b in (1, 16, 64)},
+    # batches between the listed ones, for measuring where the layer's kernel
+    # choices should switch
+    **{f"q235_b{b}": Workload(f"q235_b{b}", SHAPES["q235"], b) for b in (8, 12, 20, 24, 32, 40, 48)},
+    **{f"dsv3_b{b}": Workload(f"dsv3_b{b}", SHAPES["dsv3"], b) for b in (24, 32, 48)},
+    **{f"mixtral_b{b}": Workload(f"mixtral_b{b}", SHAPES["mixtral"], b) for b in (2, 4, 8)},
+    **{f"q30_uniform_b{b}": Workload(f"q30_uniform_b{b}", SHAPES["q30"], b) for b in (24, 40, 48, 56)},
 }
 
 

@@ -204,7 +204,9 @@ def test_layer_gate_up_kernel_rule():
                          (4096, 14336, 8, 2), (256, 128, 8, 2), (768, 192, 5, 3)]:
         sh = ops.make_shape(H, I, E, k)
         for B in (1, 2, 5, 16, 17, 39, 40, 64, 65, 256):
-            want = "grouped" if (2 * B * k >= 5 * E and H % 256 == 0 and I % 64 == 0) else "per_token"
+            P = B * k
+            shared = (2 * P >= 3 * E) if H >= 4096 else (2 * P >= 5 * E)
+            want = "grouped" if (shared and H % 256 == 0 and I % 64 == 0 and E <= 256) else "per_token"
             assert ops.layer_gate_up_kernel(sh, B) == want, (H, I, E, k, B)
     # misaligned scales keep the per-token kernel; a bad shape is an error
     w = ops.MoeWeights(256, 0x1001, 256, 256)
@@ -216,7 +218,8 @@ def test_layer_gate_up_kernel_rule():
 
 
 def test_layer_down_kernel_choice():
-    """The layer's down kernel: the expert-grouped one from B * top_k >= 3E when
+    """The layer's down kernel: the expert-grouped one from 2.5E pairs (2E for
+    rows of 6144 and more) when
     it takes the shape (I % 256 == 0, E <= 256) and batch (up to 64 tokens for
     these shapes; never beyond 128), the per-token one otherwise; the library
     answers on the host, without a GPU."""
@@ -224,8 +227,10 @@ def test_layer_down_kernel_choice():
                          (4096, 14336, 8, 2), (256, 128, 8, 2), (64, 256, 6, 3),
                          (2048, 768, 257, 8)]:
         sh = ops.make_shape(H, I, E, k)
-        for B in (1, 2, 3, 15, 16, 17, 32, 47, 48, 64, 129, 256):
-            want = "grouped" if (B * k >= 3 * E and I % 256 == 0 and E <= 256 and B <= 64) \
+        for B in (1, 2, 3, 9, 10, 15, 16, 17, 32, 39, 40, 63, 64, 129, 256):
+            P = B * k
+            shared = (P >= 2 * E) if H >= 6144 else (2 * P >= 5 * E)
+            want = "grouped" if (shared and I % 256 == 0 and E <= 256 and B <= 64) \
                 else "per_token"
             assert ops.layer_down_kernel(sh, B) == want, (H, I, E, k, B)
     # misaligned down scales keep the per-token kernel; NULL weight arrays and

@@ -98,19 +98,19 @@ def test_grouped_down_layer_sampled_tokens(q30, B):
     _check_y(y.cpu().numpy()[sample], y_ref)
 
 
-def test_layer_switches_down_kernel_at_top_k_times_b_equal_3e(q30):
-    """moe_layer's y equals moe_down's below B * top_k = 3E and
-    moe_down_grouped's from there on (Qwen-3-30B-A3B shape: 48 tokens), bit for
+def test_layer_switches_down_kernel_at_2_5e_pairs(q30):
+    """moe_layer's y equals moe_down's below 2 * B * top_k = 5E and
+    moe_down_grouped's from there on (Qwen-3-30B-A3B shape: 40 tokens), bit for
     bit, on the intermediate the layer itself produced."""
-    for B in (47, 48):
+    for B in (39, 40):
         x, ids, w = workload.tokens(q30.shape, B, batch=600 + B)
         h = torch.empty((B, 8, q30.shape.I), dtype=torch.int16, device="cuda")
         y = torch.empty((B, q30.shape.H), dtype=torch.float32, device="cuda")
         ops.moe_layer(q30.dev, _dev(x.view(np.int16)), _dev(ids), _dev(w), h, y)
         torch.cuda.synchronize()
         hb = h.cpu().numpy().view(np.uint16)
-        want = _down(q30, hb, ids, w, grouped=(B * 8 >= 3 * 128))
-        assert ops.layer_down_kernel(q30.sh, B, q30.dev) == ("grouped" if B * 8 >= 3 * 128 else "per_token")
+        want = _down(q30, hb, ids, w, grouped=(2 * B * 8 >= 5 * 128))
+        assert ops.layer_down_kernel(q30.sh, B, q30.dev) == ("grouped" if 2 * B * 8 >= 5 * 128 else "per_token")
         assert np.array_equal(y.cpu().numpy(), want), B
 
 
@@ -148,7 +148,7 @@ def test_hot_expert_duplicates_invalid_ids_and_empty_tokens(small):
     assert np.all(y[5] == 0.0)
     d, cos = parity_stats(y, y_ref)
     assert d <= DOWN_ABS, d
-    # and the layer as a whole (B * top_k >= 3E: grouped down)
+    # and the layer as a whole (2 * B * top_k >= 5E: grouped down)
     h = torch.empty((B, s.top_k, s.I), dtype=torch.int16, device="cuda")
     yl = torch.empty((B, s.H), dtype=torch.float32, device="cuda")
     err.zero_()
