@@ -160,6 +160,8 @@ def rank_seed(seed: int, rank: int) -> int:
 
 # ----------------------------------------------------------------- clocks --
 
+SOAK_S = 0.3  # seconds of untimed steps before the warm-up, for the clock record
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples every 20 ms, timestamped; started
     before the warm-up (nvidia-smi takes a moment to start) and stopped after
@@ -207,8 +209,10 @@ class ClockSampler:
                 pass
         return None
 
-    def summary(self, t0: float, t1: float):
-        sm, mx, reasons, power = [], None, set(), []
+    def summary(self, t0: float, t1: float, timed=None, soak_s=None):
+        """Samples taken from t0 to t1 (host wall clock). timed: the timed
+        region inside that window, whose own sample count is reported."""
+        sm, mx, reasons, power, in_timed = [], None, set(), [], 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in self.lines:
             f = [x.strip() for x in l.split(",")]
@@ -223,6 +227,8 @@ class ClockSampler:
             if when is None or not (t0 <= when <= t1):  # outside the timed region
                 continue
             sm.append(clk)
+            if timed is not None and timed[0] <= when <= timed[1]:
+                in_timed += 1
             try:
                 power.append(float(f[3]))
             except ValueError:
@@ -230,10 +236,14 @@ class ClockSampler:
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+        extra = {}
+        if timed is not None:
+            extra = {"window": f"a {soak_s:g} s soak of the same step, the warm-up and the timed "
+                               "region, back to back", "samples_in_timed_region": in_timed}
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0, **extra}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power) if power else None}
+                "samples": len(sm), "power_w_max": max(power) if power else None, **extra}
 
 
 # ---------------------------------------------------------- workload setup --
@@ -409,6 +419,16 @@ def run_ours(args, wl, rank, world, local_rank):
         gpu_id = str(local_rank)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(gpu_id) as clk:
+        # A soak of the same step right before the warm-up and the timed region:
+        # K steps take a few ms, shorter than the sampler's period, so the
+        # clock record covers the soak and the timed region together.
+        soak0 = time.time()
+        i = 0
+        while time.time() - soak0 < SOAK_S:
+            for _ in range(64):
+                step(i)
+                i += 1
+            torch.cuda.synchronize(dev)
         for i in range(max(3, args.warmup)):
             step(i)
         barrier()
@@ -558,7 +578,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "sweep": sweep,
         "accuracy": acc,
         "gpu_launches": 2 * args.steps,
-        "clocks": clk.summary(wall0, wall1),
+        "clocks": clk.summary(soak0, wall1, timed=(wall0, wall1), soak_s=SOAK_S),
     }
     print(json.dumps(out), flush=True)
 
