@@ -23,13 +23,20 @@
  * decoding each weight once; each output is still written once, with the
  * same numerics up to FP32 rounding order.
  *
- * LAYER KERNEL CHOICE (moe_layer, moe_layer_host, moe_layer_noalloc,
- * moe_layer_routed with ids_out), with P = B * top_k routed pairs, measured
- * on GB300 under uniform routing:
+ * LAYER KERNEL CHOICE (moe_layer, moe_layer_noalloc, moe_layer_routed with
+ * ids_out), with P = B * top_k routed pairs, measured on GB300 under uniform
+ * routing:
  *   gate/up grouped when 2P >= 5E (H < 4096), 2P >= 3E (H >= 4096);
  *   down grouped when    2P >= 5E (H < 6144), P >= 2E (H >= 6144);
  * each only where the grouped kernel takes the shape and batch. The choice
  * is reported by moe_layer_gate_up_kernel and moe_layer_down_kernel.
+ * moe_layer_host has the ids on the host and counts the batch's distinct
+ * valid experts U instead (E <= 256):
+ *   gate/up grouped when P >= 2.6 U (H < 4096), P >= 1.75 U (H >= 4096);
+ *   down grouped when    P >= 2.6 U (H < 6144), P >= 2.2 U (H >= 6144);
+ * the same break-even points under uniform routing, and earlier where the
+ * pairs crowd onto few experts (skewed routing); moe_layer_host_kernels
+ * reports that choice.
  *
  * Numerics (fixed by this API):
  *   g = sum_h x[t,h] Wg[e,n,h],  u = sum_h x[t,h] Wu[e,n,h]     (FP32 accum.)
@@ -220,6 +227,18 @@ moe_status moe_layer_down_kernel(const moe_shape* shape, const moe_weights* w, i
                                  int32_t* kernel_out);
 
 /*
+ * moe_layer_host_kernels -- the kernels moe_layer_host runs for a batch whose
+ * ids_host [B][top_k] are given (host memory): *gate_up_out and *down_out =
+ * 0 for the per-token kernel, 1 for the expert-grouped one (LAYER KERNEL
+ * CHOICE above). Host-only; `w` may be NULL (scales taken to be aligned);
+ * MOE_ERR_SHAPE for a bad shape, MOE_ERR_NULL for a NULL shape, output or
+ * (B > 0) ids_host.
+ */
+moe_status moe_layer_host_kernels(const moe_shape* shape, const moe_weights* w,
+                                  const int32_t* ids_host, int32_t B, int32_t* gate_up_out,
+                                  int32_t* down_out);
+
+/*
  * moe_layer -- the whole layer: the gate/up step then moe_down on `stream`.
  * Each step runs its per-token or its expert-grouped kernel as the LAYER
  * KERNEL CHOICE above says.
@@ -234,10 +253,12 @@ moe_status moe_layer(const moe_shape* shape, const moe_weights* w, const uint16_
 /*
  * moe_layer_host -- the layer end to end from HOST buffers: copies x, ids and
  * wts host->device into the caller's device staging buffers (one
- * cudaMemcpyAsync each), runs moe_layer, and copies y device->host, all
- * enqueued on `stream`. Returns once enqueued: synchronise `stream` before
- * reading y_host. Host buffers should be pinned for the copies to be
- * asynchronous. Shapes and device-buffer rules as for moe_layer.
+ * cudaMemcpyAsync each), runs the layer as moe_layer does with the kernels
+ * chosen from ids_host (LAYER KERNEL CHOICE above), and copies y
+ * device->host, all enqueued on `stream`. Returns once enqueued: synchronise
+ * `stream` before reading y_host. Host buffers should be pinned for the
+ * copies to be asynchronous. Shapes and device-buffer rules as for
+ * moe_layer.
  */
 moe_status moe_layer_host(const moe_shape* shape, const moe_weights* w, const uint16_t* x_host,
                           const int32_t* ids_host, const float* wts_host, int32_t B,

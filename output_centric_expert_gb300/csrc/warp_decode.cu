@@ -216,6 +216,58 @@ DownForm layer_down_form(const moe_shape* s, const moe_weights* w, int32_t B) {
   return DownForm::kPerToken;
 }
 
+// The forms for a batch whose ids are on the host: the same measured
+// break-even points written as pairs per used expert, P >= tau * U with U the
+// distinct experts of the batch, so that a batch whose pairs crowd onto few
+// experts (skewed routing) takes the grouped kernels where they win. With
+// uniform routing U = E (1 - (1 - k/E)^B) on average, and the thresholds
+// reproduce the rules on P and E at the measured shapes: gate/up tau = 2.6
+// (H < 4096; Qwen-3-30B-A3B: 2.49 pairs per used expert at its 36-token
+// break-even, 2.71 at 40 tokens) or 1.75 (H >= 4096; Qwen-3-235B-A22B 1.69 at
+// 19 tokens, Mixtral shape 1.64 at 5, DeepSeek-V3 shape 1.88 at 46); down
+// tau = 2.6 (H < 6144) or 2.2 (H >= 6144; DeepSeek-V3 shape 2.1 at 55
+// tokens). Skewed Qwen-3-30B-A3B batch of 32 tokens (43 used experts, 6 pairs
+// each): gate/up 45.0 us grouped against 73.8 per-token, down 34.9 against
+// 38.4.
+struct LayerForms {
+  GateUpForm gate_up;
+  DownForm down;
+};
+
+LayerForms layer_forms_for_ids(const moe_shape* s, const moe_weights* w, const int32_t* ids,
+                               int32_t B) {
+  LayerForms f = {GateUpForm::kPerToken, DownForm::kPerToken};
+  if (s->E > kRouteMaxE) return f;  // beyond the grouped kernels' expert count
+  uint64_t used[kRouteMaxE / 64] = {};
+  const int64_t P = (int64_t)B * s->top_k;
+  int64_t U = 0;
+  for (int64_t p = 0; p < P; ++p) {
+    const int32_t e = ids[p];
+    if (e < 0 || e >= s->E) continue;
+    const uint64_t bit = 1ull << (e & 63);
+    if (!(used[e >> 6] & bit)) {
+      used[e >> 6] |= bit;
+      ++U;
+    }
+  }
+  if (U == 0) return f;
+  const bool gu_shared = s->H >= 4096 ? 4 * P >= 7 * U : 5 * P >= 13 * U;
+  const bool dn_shared = s->H >= 6144 ? 5 * P >= 11 * U : 5 * P >= 13 * U;
+  if (gu_shared && gate_up_grouped_supported(s, w, B)) f.gate_up = GateUpForm::kGrouped;
+  if (dn_shared && down_grouped_supported(s, w, B)) f.down = DownForm::kGrouped;
+  return f;
+}
+
+// The layer with the given forms (arguments validated by the caller): the
+// down kernel is launched as a programmatic dependent of the gate/up kernel.
+moe_status layer_run(const moe_shape* s, const moe_weights* w, const uint16_t* x,
+                     const int32_t* ids, const float* wts, int32_t B, uint16_t* h, float* y,
+                     int32_t* err, cudaStream_t st, LayerForms f) {
+  moe_status rc = gate_up_impl(s, w, x, ids, B, h, err, st, kNoRoute, f.gate_up);
+  if (rc != MOE_OK) return rc;
+  return down_impl(s, w, h, ids, wts, B, y, err, st, true, nullptr, f.down);
+}
+
 }  // namespace
 }  // namespace wd
 
@@ -271,6 +323,22 @@ extern "C" moe_status moe_layer_down_kernel(const moe_shape* shape, const moe_we
   return MOE_OK;
 }
 
+extern "C" moe_status moe_layer_host_kernels(const moe_shape* shape, const moe_weights* w,
+                                             const int32_t* ids_host, int32_t B,
+                                             int32_t* gate_up_out, int32_t* down_out) {
+  using namespace wd;
+  if (!gate_up_out || !down_out) return MOE_ERR_NULL;
+  moe_status rc = check_shape(shape, B);
+  if (rc != MOE_OK) return rc;
+  if (w && (rc = check_weights(w, true, true)) != MOE_OK) return rc;
+  if (B > 0 && !ids_host) return MOE_ERR_NULL;
+  const LayerForms f = B > 0 ? layer_forms_for_ids(shape, w, ids_host, B)
+                             : LayerForms{GateUpForm::kPerToken, DownForm::kPerToken};
+  *gate_up_out = f.gate_up == GateUpForm::kGrouped ? 1 : 0;
+  *down_out = f.down == DownForm::kGrouped ? 1 : 0;
+  return MOE_OK;
+}
+
 extern "C" moe_status moe_layer(const moe_shape* shape, const moe_weights* w, const uint16_t* x,
                                 const int32_t* ids, const float* wts, int32_t B,
                                 uint16_t* h_scratch, float* y, int32_t* err_flag,
@@ -282,11 +350,8 @@ extern "C" moe_status moe_layer(const moe_shape* shape, const moe_weights* w, co
   if ((rc = check_weights(w, true, true)) != MOE_OK) return rc;
   if (B == 0) return MOE_OK;
   if (!x || !ids || !wts || !h_scratch || !y) return MOE_ERR_NULL;
-  rc = gate_up_impl(shape, w, x, ids, B, h_scratch, err_flag, (cudaStream_t)stream, kNoRoute,
-                    layer_form(shape, w, B));
-  if (rc != MOE_OK) return rc;
-  return down_impl(shape, w, h_scratch, ids, wts, B, y, err_flag, (cudaStream_t)stream, true,
-                   nullptr, layer_down_form(shape, w, B));
+  return layer_run(shape, w, x, ids, wts, B, h_scratch, y, err_flag, (cudaStream_t)stream,
+                   {layer_form(shape, w, B), layer_down_form(shape, w, B)});
 }
 
 extern "C" moe_status moe_route(const moe_shape* shape, const float* logits, int32_t B,
@@ -359,7 +424,7 @@ extern "C" moe_status moe_layer_host(const moe_shape* shape, const moe_weights* 
       !y_dev)
     return MOE_ERR_NULL;
   if (!aligned(x_dev, 16) || !aligned(h_dev, 16) || !aligned(ids_dev, 4) ||
-      !aligned(wts_dev, 4) || !aligned(y_dev, 4)) {
+      !aligned(wts_dev, 4) || !aligned(y_dev, 4) || !aligned(err_flag, 4)) {
     set_error_msg("alignment: x_dev and h_dev need 16 bytes, others 4");
     return MOE_ERR_ALIGN;
   }
@@ -373,7 +438,10 @@ extern "C" moe_status moe_layer_host(const moe_shape* shape, const moe_weights* 
     set_error("moe_layer_host: host->device copy", e);
     return MOE_ERR_CUDA;
   }
-  rc = moe_layer(shape, w, x_dev, ids_dev, wts_dev, B, h_dev, y_dev, err_flag, stream);
+  // the ids are on the host: the kernels are chosen from the batch's own
+  // pairs per used expert
+  rc = layer_run(shape, w, x_dev, ids_dev, wts_dev, B, h_dev, y_dev, err_flag, st,
+                 layer_forms_for_ids(shape, w, ids_host, B));
   if (rc != MOE_OK) return rc;
   if ((e = cudaMemcpyAsync(y_host, y_dev, nx * 4, cudaMemcpyDeviceToHost, st)) != cudaSuccess) {
     set_error("moe_layer_host: device->host copy", e);

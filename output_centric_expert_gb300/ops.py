@@ -63,6 +63,9 @@ def lib() -> ctypes.CDLL:
         L.moe_down_grouped.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp]
         L.moe_layer_down_kernel.restype = ctypes.c_int
         L.moe_layer_down_kernel.argtypes = [sp, wp, i32, ctypes.POINTER(ctypes.c_int32)]
+        L.moe_layer_host_kernels.restype = ctypes.c_int
+        L.moe_layer_host_kernels.argtypes = [sp, wp, vp, i32, ctypes.POINTER(ctypes.c_int32),
+                                             ctypes.POINTER(ctypes.c_int32)]
         L.moe_layer.restype = ctypes.c_int
         L.moe_layer.argtypes = [sp, wp, vp, vp, vp, i32, vp, vp, vp, vp]
         L.moe_route.restype = ctypes.c_int
@@ -250,6 +253,20 @@ def layer_down_kernel(shape: MoeShape, B: int, weights: "DeviceWeights | None" =
     return "grouped" if out.value == 1 else "per_token"
 
 
+def layer_host_kernels(shape: MoeShape, ids_host: np.ndarray,
+                       weights: "DeviceWeights | None" = None) -> tuple[str, str]:
+    """The (gate/up, down) kernels moe_layer_host runs for a batch whose ids are
+    given on the host (moe_layer_host_kernels): each "per_token" or "grouped"."""
+    ids_host = np.ascontiguousarray(ids_host, dtype=np.int32)
+    B = ids_host.shape[0] if ids_host.ndim else 0
+    gu, dn = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    _check("moe_layer_host_kernels", lib().moe_layer_host_kernels(
+        ctypes.byref(shape), ctypes.byref(weights.struct) if weights is not None else None,
+        ids_host.ctypes.data_as(ctypes.c_void_p), B, ctypes.byref(gu), ctypes.byref(dn)))
+    name = {0: "per_token", 1: "grouped"}
+    return name[gu.value], name[dn.value]
+
+
 def moe_layer(weights: DeviceWeights, x: torch.Tensor, ids: torch.Tensor, wts: torch.Tensor,
               h_scratch: torch.Tensor, y: torch.Tensor, err_flag: torch.Tensor | None = None,
               stream=None) -> torch.Tensor:
@@ -342,6 +359,6 @@ def exported_symbols() -> list[str]:
     """The entry points include/warp_decode.h declares."""
     return ["moe_packed_bytes", "moe_pack_weights", "moe_gate_up", "moe_gate_up_grouped",
             "moe_layer_gate_up_kernel", "moe_down", "moe_down_grouped",
-            "moe_layer_down_kernel", "moe_layer",
+            "moe_layer_down_kernel", "moe_layer_host_kernels", "moe_layer",
             "moe_layer_host", "moe_layer_noalloc", "moe_route", "moe_layer_routed",
             "moe_local_ids", "moe_status_string", "moe_last_error"]

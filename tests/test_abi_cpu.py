@@ -145,7 +145,8 @@ typedef void (*any_fn)(void);
 static const any_fn entry_points[] = {
   (any_fn)moe_packed_bytes, (any_fn)moe_pack_weights, (any_fn)moe_gate_up,
   (any_fn)moe_gate_up_grouped, (any_fn)moe_layer_gate_up_kernel, (any_fn)moe_down,
-  (any_fn)moe_down_grouped, (any_fn)moe_layer_down_kernel, (any_fn)moe_layer, (any_fn)moe_layer_host, (any_fn)moe_route, (any_fn)moe_layer_routed,
+  (any_fn)moe_down_grouped, (any_fn)moe_layer_down_kernel, (any_fn)moe_layer_host_kernels,
+  (any_fn)moe_layer, (any_fn)moe_layer_host, (any_fn)moe_route, (any_fn)moe_layer_routed,
   (any_fn)moe_layer_noalloc, (any_fn)moe_local_ids, (any_fn)moe_status_string,
   (any_fn)moe_last_error,
 };
@@ -215,6 +216,53 @@ def test_layer_gate_up_kernel_rule():
                                               ctypes.byref(out)) == 0 and out.value == 0
     with pytest.raises(ops.WarpDecodeError):
         ops.layer_gate_up_kernel(ops.make_shape(100, 768, 128, 8), 64)
+
+
+def test_layer_host_kernel_choice():
+    """moe_layer_host picks its kernels from the batch's own ids: pairs per used
+    expert against the measured break-even points. Uniform routing gives the
+    same choice as the rules on B (Qwen-3-30B-A3B shape: per-token at 32 tokens,
+    grouped from 40); a skewed batch of 32 tokens, its pairs on a few dozen
+    experts, takes the grouped kernels; all on one expert likewise; no valid id
+    keeps the per-token kernels. Host-only."""
+    from output_centric_expert_gb300 import workload
+    q30 = workload.SHAPES["q30"]
+    sh = ops.make_shape(q30.H, q30.I, q30.E, q30.top_k)
+    for B in (8, 16, 32, 36):
+        ids = workload.tokens(q30, B, seed=0, batch=0, routing="uniform")[1]
+        assert ops.layer_host_kernels(sh, ids) == ("per_token", "per_token"), B
+    for B in (40, 48, 64):
+        ids = workload.tokens(q30, B, seed=0, batch=0, routing="uniform")[1]
+        assert ops.layer_host_kernels(sh, ids) == ("grouped", "grouped"), B
+        assert ops.layer_gate_up_kernel(sh, B) == "grouped" and ops.layer_down_kernel(sh, B) == "grouped"
+    for b in range(4):
+        ids = workload.tokens(q30, 32, seed=0, batch=b, routing="skewed")[1]
+        U = len(np.unique(ids))
+        assert 256 >= 2.6 * U, U  # the skewed batches crowd onto few experts
+        assert ops.layer_host_kernels(sh, ids) == ("grouped", "grouped")
+    one = np.full((8, 8), 5, dtype=np.int32)  # 64 pairs on expert 5 (duplicates within tokens)
+    assert ops.layer_host_kernels(sh, one) == ("grouped", "grouped")
+    none = np.full((8, 8), -1, dtype=np.int32)
+    assert ops.layer_host_kernels(sh, none) == ("per_token", "per_token")
+    # the thresholds in pairs per used expert, at a boundary: 13 pairs on 5 experts
+    # is 2.6 per expert (grouped), 12 on 5 is 2.4 (per-token); top_k = 1
+    sh1 = ops.make_shape(2048, 768, 128, 1)
+    ids13 = np.array([[e] for e in [0, 1, 2, 3, 4] * 2 + [0, 1, 2]], dtype=np.int32)
+    ids12 = ids13[:12]
+    assert ops.layer_host_kernels(sh1, ids13) == ("grouped", "grouped")
+    assert ops.layer_host_kernels(sh1, ids12) == ("per_token", "per_token")
+    # longer rows: gate/up from 1.75 pairs per expert (H >= 4096), down from 2.2 (H >= 6144)
+    sh4 = ops.make_shape(4096, 1536, 128, 1)
+    ids9 = np.array([[e] for e in [0, 1, 2, 3] * 2 + [0]], dtype=np.int32)  # 9 on 4: 2.25
+    assert ops.layer_host_kernels(sh4, ids9) == ("grouped", "per_token")
+    sh7 = ops.make_shape(7168, 2048, 256, 1)
+    assert ops.layer_host_kernels(sh7, ids9) == ("grouped", "grouped")
+    assert ops.layer_host_kernels(sh7, ids9[:8]) == ("grouped", "per_token")  # 2.0 per expert
+    # E > 256: beyond the grouped kernels
+    big = ops.make_shape(2048, 768, 257, 8)
+    assert ops.layer_host_kernels(big, one) == ("per_token", "per_token")
+    with pytest.raises(ops.WarpDecodeError):
+        ops.layer_host_kernels(ops.make_shape(100, 768, 128, 8), one)
 
 
 def test_layer_down_kernel_choice():

@@ -114,6 +114,42 @@ def test_layer_switches_down_kernel_at_2_5e_pairs(q30):
         assert np.array_equal(y.cpu().numpy(), want), B
 
 
+@pytest.mark.parametrize("B,routing,batch", [(32, "skewed", 0), (32, "skewed", 3), (16, "skewed", 1),
+                                             (32, "uniform", 0), (40, "uniform", 2)])
+def test_host_entry_point_chooses_from_its_ids(q30, B, routing, batch):
+    """moe_layer_host picks its kernels from the batch's own ids (pairs per used
+    expert): a skewed batch of 32 tokens runs the grouped kernels although
+    moe_layer, which decides on B, runs the per-token ones there. Its y equals,
+    bit for bit, the kernels it reports run one after the other on the same
+    device inputs, and the oracle on sampled tokens."""
+    x, ids, w = workload.tokens(q30.shape, B, routing=routing, batch=batch)
+    gu, dn = ops.layer_host_kernels(q30.sh, ids, q30.dev)
+    if routing == "skewed" and B == 32:
+        assert (gu, dn) == ("grouped", "grouped")
+    if routing == "uniform":
+        assert (gu, dn) == (ops.layer_gate_up_kernel(q30.sh, B), ops.layer_down_kernel(q30.sh, B))
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    xh, idh, wh = pin(x.view(np.int16)), pin(ids), pin(w)
+    yh = torch.full((B, q30.shape.H), float("nan"), dtype=torch.float32).pin_memory()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev = dict(x_dev=torch.empty_like(xh, device="cuda"), ids_dev=torch.empty_like(idh, device="cuda"),
+               wts_dev=torch.empty_like(wh, device="cuda"),
+               h_dev=torch.empty((B, 8, q30.shape.I), dtype=torch.int16, device="cuda"),
+               y_dev=torch.empty((B, q30.shape.H), dtype=torch.float32, device="cuda"))
+    ops.moe_layer_host(q30.dev, xh, idh, wh, y_host=yh, err_flag=err, **dev)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    h = torch.empty((B, 8, q30.shape.I), dtype=torch.int16, device="cuda")
+    (ops.moe_gate_up_grouped if gu == "grouped" else ops.moe_gate_up)(
+        q30.dev, _dev(x.view(np.int16)), _dev(ids), h)
+    torch.cuda.synchronize()
+    want = _down(q30, h.cpu().numpy().view(np.uint16), ids, w, grouped=(dn == "grouped"))
+    assert np.array_equal(yh.numpy(), want)
+    sample = sorted({0, B // 2, B - 1})
+    y_ref, _ = oracle.moe_layer(q30.ref, x[sample], ids[sample], w[sample])
+    _check_y(yh.numpy()[sample], y_ref)
+
+
 def test_grouped_down_deterministic(q30):
     x, ids, w = workload.tokens(q30.shape, 48, routing="skewed", batch=7)
     h = _gpu_h(q30, x, ids)
