@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="q30_b32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak", type=float, default=SOAK_S,
+                    help="seconds of untimed steps before the warm-up, so that the clock "
+                         "samples cover the load of the timed region (0: none, e.g. under ncu)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="leave out the B=1..64 sweep and accuracy keys of the contract line")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -462,7 +465,7 @@ def run_ours(args, wl, rank, world, local_rank):
         # clock record covers the soak and the timed region together.
         soak0 = time.time()
         i = 0
-        while time.time() - soak0 < SOAK_S:
+        while time.time() - soak0 < args.soak:
             for _ in range(64):
                 step(i)
                 i += 1
@@ -626,7 +629,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "sweep": sweep,
         "accuracy": acc,
         "gpu_launches": 2 * args.steps,
-        "clocks": clk.summary(soak0, wall1, timed=(wall0, wall1), soak_s=SOAK_S),
+        "clocks": clk.summary(soak0, wall1, timed=(wall0, wall1), soak_s=args.soak),
     }
     print(json.dumps(out), flush=True)
 
