@@ -165,8 +165,9 @@ moe_status moe_gate_up_grouped(const moe_shape* shape, const moe_weights* w,
 
 /*
  * moe_layer_gate_up_kernel -- which kernel the layer entry points (moe_layer,
- * moe_layer_host, moe_layer_noalloc, moe_layer_routed with ids_out) run for
- * the gate/up step of a batch of B tokens: *kernel_out = 0 for moe_gate_up's
+ * moe_layer_noalloc, moe_layer_routed with ids_out; moe_layer_host decides
+ * from its ids, see moe_layer_host_kernels) run for the gate/up step of a
+ * batch of B tokens: *kernel_out = 0 for moe_gate_up's
  * per-token kernel, 1 for moe_gate_up_grouped's. A token's results can differ
  * in FP32 rounding order between the two, never beyond that. `w` may be NULL,
  * in which case gu_scales is taken to be suitably aligned; a non-NULL `w` has
@@ -217,8 +218,8 @@ moe_status moe_down_grouped(const moe_shape* shape, const moe_weights* w, const 
 
 /*
  * moe_layer_down_kernel -- which kernel the layer entry points (moe_layer,
- * moe_layer_host, moe_layer_noalloc, moe_layer_routed with ids_out) run for
- * the down step of a batch of B tokens: *kernel_out = 0 for moe_down's
+ * moe_layer_noalloc, moe_layer_routed with ids_out) run for the down step of
+ * a batch of B tokens: *kernel_out = 0 for moe_down's
  * per-token kernel, 1 for moe_down_grouped's. Host-only; `w` may be NULL (the
  * scales are then taken to be aligned); errors as for moe_layer_gate_up_kernel,
  * with the down arrays of a non-NULL `w` checked.
