@@ -14,7 +14,9 @@
 //   CTA c owns rows o0 = 16c .. o0+15 of y for all B tokens. The batch's
 //   (token, slot) pairs are listed by expert, in pair order, and cut into
 //   passes of up to 8 pairs of one expert; the CTA's 12 warps take the passes
-//   in turn (pass j goes to warp j mod 12). For a pass of expert e a warp
+//   in turn (pass j goes to warp j mod 12; when the CTA has fewer than 3
+//   passes per warp, as with a few wide experts, each pass is cut into chunks
+//   of its row and the warps take the chunks). For a pass of expert e a warp
 //   streams rows o0..o0+15 of e's down matrix (MMA rows 0..15) against the
 //   intermediate rows of the pass's pairs (the MMA's 8 columns), one
 //   mma.sync.m16n8k16 (f16 x f16 -> FP32) per 16 elements. Per 32-element
@@ -267,9 +269,17 @@ __global__ void __launch_bounds__(kDgThreads, 1)
   __syncthreads();
   const int npass = *s_nused;
   const int nck = I / kDgChunk;
+  // Work items: a pass, or when the CTA has fewer than 3 passes per warp
+  // (few wide experts, e.g. Mixtral-shaped I = 14336 with 16 passes), a
+  // chunk of its steps, so that every warp has work; each item's sums are
+  // added into the partial y of the warp that ran it.
+  const int want = (3 * kDgWarps + npass - 1) / max(npass, 1);
+  const int spc = (nck + min(nck, max(1, want)) - 1) / min(nck, max(1, want));  // steps per item
+  const int nch = (nck + spc - 1) / spc;  // items per pass
+  const int nitem = npass * nch;
 
-  // ---- the warp's passes (up to 8 pairs of one expert each): warp,
-  // warp + kDgWarps, ...; each pass in steps of 256 row elements ----
+  // ---- the warp's items (a pass of up to 8 pairs of one expert, or a chunk
+  // of it): warp, warp + kDgWarps, ...; each in steps of 256 row elements ----
   uint8_t* my_h = s_h + (size_t)warp * 2 * kDgCols * kDgColBytes;
   int* my_sig = s_sig + warp * 2 * kDgCols;
   float* my_y = s_y + (size_t)warp * B * kDgRows;
@@ -402,22 +412,30 @@ __global__ void __launch_bounds__(kDgThreads, 1)
   // Pipeline: step k computes from register buffer k % 2 and shared buffer
   // k % 2; the codes and intermediate rows of step k + 1 are requested at its
   // start into the other buffers.
-  int pi = warp, kc = 0;  // the warp's current pass and step
+  auto item_k0 = [&](int i) { return (i - (i / nch) * nch) * spc; };
+  int it = warp, kc = 0;  // the warp's current item and step
   DgBuf W0, W1;
-  if (pi < npass) wload(s_pass[pi].x, 0, W0);  // the first codes, before the wait
+  if (it < nitem) {  // the first codes, before the wait
+    kc = item_k0(it);
+    wload(s_pass[it / nch].x, kc, W0);
+  }
   wait_prerequisite();  // the intermediate h is complete from here on
-  if (pi < npass) {
-    int4 ps = s_pass[pi];
-    hload(ps, 0, 0);
+  if (it < nitem) {
+    int4 ps = s_pass[it / nch];
+    int kend = min(nck, kc + spc);
+    hload(ps, kc, 0);
     int buf = 0;
     auto step = [&](DgBuf& Wc, DgBuf& Wn) -> bool {
-      int pn = pi, kn = kc + 1;
-      if (kn == nck) {
-        kn = 0;
-        pn += kDgWarps;
+      int in = it, kn = kc + 1, kendn = kend;
+      const bool last = kn == kend;  // this step ends the item
+      if (last) in = it + kDgWarps;
+      const bool more = in < nitem;
+      int4 nps = ps;
+      if (last && more) {
+        nps = s_pass[in / nch];
+        kn = item_k0(in);
+        kendn = min(nck, kn + spc);
       }
-      const bool more = pn < npass;
-      const int4 nps = more ? s_pass[pn] : ps;
       __syncwarp();  // every lane has finished reading the buffers being refilled
       if (more) {
         wload(nps.x, kn, Wn);
@@ -430,9 +448,10 @@ __global__ void __launch_bounds__(kDgThreads, 1)
       hconvert(ps.z, buf);
       __syncwarp();
       compute(Wc, buf);
-      if (kn == 0) flush(ps);
-      pi = pn;
+      if (last) flush(ps);
+      it = in;
       kc = kn;
+      kend = kendn;
       ps = nps;
       buf ^= 1;
       return more;
