@@ -505,6 +505,10 @@ def run_ours(args, wl, rank, world, local_rank):
     gu_form = ops.layer_gate_up_kernel(layers[0].shape, wl.B, layers[0])
     gu_kernel = "moe_gate_up_grouped" if gu_form == "grouped" else "moe_gate_up"
     gate_up_fn = getattr(ops, gu_kernel)
+    # and the down kernel it runs
+    dn_kernel = ("moe_down_grouped" if ops.layer_down_kernel(layers[0].shape, wl.B, layers[0])
+                 == "grouped" else "moe_down")
+    down_fn = getattr(ops, dn_kernel)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     barrier()
     for i in range(args.steps):
@@ -513,7 +517,7 @@ def run_ours(args, wl, rank, world, local_rank):
         evs[i][0].record(stream)
         gate_up_fn(L, dx[b], dids[b], h, err, stream)
         evs[i][1].record(stream)
-        ops.moe_down(L, h, dids[b], dw[b], y, err, stream)
+        down_fn(L, h, dids[b], dw[b], y, err, stream)
         evs[i][2].record(stream)
     barrier()
     gu_ms = [e[0].elapsed_time(e[1]) for e in evs]
@@ -608,7 +612,8 @@ def run_ours(args, wl, rank, world, local_rank):
                    "layer_bytes_per_step": sum(lay_bytes) / args.steps,
                    "gate_up_us": sum(gu_ms) / args.steps * 1e3,
                    "down_us": sum(dn_ms) / args.steps * 1e3,
-                   "down_gbs": dn_gbs},
+                   "down_gbs": dn_gbs, "down_frac_of_peak": dn_gbs / peak,
+                   "down_kernel": dn_kernel},
         "roofline": {"bound": "hbm", "kernel": gu_kernel, "achieved": gu_gbs, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": gu_gbs / peak,
                      "algorithmic_bytes_per_launch": gu_launch_bytes,
