@@ -14,9 +14,9 @@
 //   CTA c owns rows o0 = 16c .. o0+15 of y for all B tokens. The batch's
 //   (token, slot) pairs are listed by expert, in pair order, and cut into
 //   passes of up to 8 pairs of one expert; the CTA's 12 warps take the passes
-//   in turn (pass j goes to warp j mod 12; when the CTA has fewer than 3
-//   passes per warp, as with a few wide experts, each pass is cut into chunks
-//   of its row and the warps take the chunks). For a pass of expert e a warp
+//   in turn (pass j goes to warp j mod 12; with a few wide experts, each pass
+//   is cut into chunks of its row and the warps take the chunks). For a pass
+//   of expert e a warp
 //   streams rows o0..o0+15 of e's down matrix (MMA rows 0..15) against the
 //   intermediate rows of the pass's pairs (the MMA's 8 columns), one
 //   mma.sync.m16n8k16 (f16 x f16 -> FP32) per 16 elements. Per 32-element
@@ -269,13 +269,16 @@ __global__ void __launch_bounds__(kDgThreads, 1)
   __syncthreads();
   const int npass = *s_nused;
   const int nck = I / kDgChunk;
-  // Work items: a pass, or when the CTA has fewer than 3 passes per warp
-  // (few wide experts, e.g. Mixtral-shaped I = 14336 with 16 passes), a
-  // chunk of its steps, so that every warp has work; each item's sums are
-  // added into the partial y of the warp that ran it.
-  const int want = (3 * kDgWarps + npass - 1) / max(npass, 1);
-  const int spc = (nck + min(nck, max(1, want)) - 1) / min(nck, max(1, want));  // steps per item
-  const int nch = (nck + spc - 1) / spc;  // items per pass
+  // Work items: a pass, or, when the CTA has fewer than 6 passes per warp
+  // (few wide experts, e.g. Mixtral-shaped I = 14336 with 16 passes per CTA),
+  // chunks of at least 4 of its steps, up to about 12 items per warp; each
+  // item's sums are added into the partial y of the warp that ran it.
+  // Measured on GB300: shorter or uneven chunks, or chunks where passes are
+  // many, cost more in per-item work than they gain in balance.
+  const int want = (12 * kDgWarps + npass - 1) / max(npass, 1);
+  const int parts = npass < 6 * kDgWarps ? max(1, min(want, nck / 4)) : 1;
+  const int spc = (nck + parts - 1) / parts;        // steps per item
+  const int nch = (nck + spc - 1) / spc;            // items per pass
   const int nitem = npass * nch;
 
   // ---- the warp's items (a pass of up to 8 pairs of one expert, or a chunk
