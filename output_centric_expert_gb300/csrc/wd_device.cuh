@@ -107,10 +107,13 @@ moe_status launch_gate_up_kernels(const moe_shape* s, const moe_weights* w, cons
                                   const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
                                   cudaStream_t st, RouteArgs route);
 // moe_gate_up with a kernel compiled for the shape's H, if there is one:
-// returns false (launching nothing) otherwise. spw: routed slots per warp.
+// returns false (launching nothing) otherwise. spw: routed slots per warp;
+// ctas_per_sm: 3, or 4 (64 registers; 2 or 4 slots per warp, H = 2048 or
+// 4096 only).
 bool launch_gate_up_fixed_h(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                             const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
-                            cudaStream_t st, RouteArgs route, int spw, moe_status* rc);
+                            cudaStream_t st, RouteArgs route, int spw, int ctas_per_sm,
+                            moe_status* rc);
 // dependent = true launches moe_down as a programmatic dependent of the kernel
 // before it on the stream (used by the layer entry points, where that kernel
 // is moe_gate_up and only h is produced by it).

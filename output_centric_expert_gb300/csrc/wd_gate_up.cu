@@ -6,13 +6,12 @@
 namespace wd {
 namespace {
 
-// Slots per warp of moe_gate_up. Small batches: the fewest that make the grid
-// a single wave at 3 CTAs per SM, as long as a warp has at most 8 (slot,
+// Slots per warp of moe_gate_up for small batches: the fewest that make the
+// grid a single wave at 3 CTAs per SM, as long as a warp has at most 8 (slot,
 // segment) units to stream one after the other (measured: Q30 B=2 19.5 ->
 // 18.1 us, B=4 29.7 -> 28.3, Q235 B=1 34.6 -> 33.0; 32 units per warp for the
-// DeepSeek-V3-shaped layer at B=1 was slower). Otherwise as many as keep at
-// least kMinCtasPerSm CTAs per SM.
-int pick_spw(int B, int top_k, int I, int nseg) {
+// DeepSeek-V3-shaped layer at B=1 was slower); 0 if there is none.
+int small_batch_spw(int B, int top_k, int I, int nseg) {
   const int sms = sm_count();
   const int small[4] = {1, 2, 4, 8};
   for (int v : small) {
@@ -20,6 +19,12 @@ int pick_spw(int B, int top_k, int I, int nseg) {
     const int64_t ctas = (int64_t)B * ((top_k + v - 1) / v) * (I / kWarpsPerCta);
     if (ctas <= 3 * sms) return v;
   }
+  return 0;
+}
+
+// Otherwise: as many as keep at least kMinCtasPerSm CTAs per SM.
+int pick_spw(int B, int top_k, int I) {
+  const int sms = sm_count();
   const int spws[4] = {8, 4, 2, 1};
   for (int v : spws) {
     if (v > top_k) continue;
@@ -59,8 +64,28 @@ moe_status launch_gate_up_kernels(const moe_shape* s, const moe_weights* w, cons
                                   cudaStream_t st, RouteArgs route) {
   moe_status rc;
   const int nseg = ((s->H >> 5) + kSegBlocks - 1) / kSegBlocks;  // 2048-element row segments
-  const int spw = pick_spw(B, s->top_k, s->I, nseg);
-  if (launch_gate_up_fixed_h(s, w, x, ids, B, h, err, st, route, spw, &rc)) return rc;
+  int spw = small_batch_spw(B, s->top_k, s->I, nseg), ctas_per_sm = 3;
+  if (spw == 0) {
+    spw = pick_spw(B, s->top_k, s->I);
+    // Rows of 2048 and 4096: 4 (slot, segment) units per warp at four CTAs
+    // per SM (64 registers) while the batch has at most 1.5 E pairs (H =
+    // 2048) or E pairs (H = 4096), and for H = 4096 then 8 units at four
+    // CTAs per SM up to 1.5 E pairs. Measured on GB300 in the layer (CUDA
+    // graph, against 8 slots per warp at three CTAs per SM): Qwen-3-30B-A3B
+    // shape B=8..24 3-6 % faster (B=16 75.1 -> 70.9 us), slower from 28
+    // tokens; Qwen-3-235B-A22B shape B=4..20 3-8 % faster (B=12 239.0 ->
+    // 221.1 us). Each intermediate is the same bit for bit.
+    const int64_t P = (int64_t)B * s->top_k, E = s->E;
+    if (s->H == 2048 && 2 * P <= 3 * E && s->top_k >= 4) {
+      spw = 4;
+      ctas_per_sm = 4;
+    } else if (s->H == 4096 && 2 * P <= 3 * E && s->top_k >= 4) {
+      spw = P <= E ? 2 : 4;
+      ctas_per_sm = 4;
+    }
+  }
+  if (launch_gate_up_fixed_h(s, w, x, ids, B, h, err, st, route, spw, ctas_per_sm, &rc))
+    return rc;
   if (nseg == 1) rc = launch_gate_up_spw<1>(s, w, x, ids, B, h, err, st, route, spw);
   else if (nseg == 2) rc = launch_gate_up_spw<2>(s, w, x, ids, B, h, err, st, route, spw);
   else rc = launch_gate_up_spw<4>(s, w, x, ids, B, h, err, st, route, spw);

@@ -29,8 +29,10 @@ struct GateUpUnit {
 // KH: the row length H fixed at compile time (0: taken from the argument). With
 // it the row strides and the activation offsets are constants, which the
 // loads take as immediates -- about 5 % fewer instructions per weight.
-template <int SPW, int NSEG, bool FULL, int KH>
-__global__ void __launch_bounds__(kThreads, 3)
+// MINB: CTAs per SM the registers are sized for (3: up to 85 per thread; 4:
+// 64, for up to 4 slots per warp).
+template <int SPW, int NSEG, bool FULL, int KH, int MINB = 3>
+__global__ void __launch_bounds__(kThreads, MINB)
     moe_gate_up_kernel(const uint8_t* __restrict__ gu_codes,
                        const uint8_t* __restrict__ gu_scales,
                        const uint16_t* __restrict__ x, const int32_t* __restrict__ ids,
@@ -135,16 +137,16 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 }
 
-template <int SPW, int NSEG, bool FULL, int KH>
+template <int SPW, int NSEG, bool FULL, int KH, int MINB = 3>
 moe_status launch_gate_up(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                           const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
                           cudaStream_t st, RouteArgs route) {
   const size_t smem = (size_t)s->H * 2;
-  moe_status rc = allow_smem(moe_gate_up_kernel<SPW, NSEG, FULL, KH>, smem);
+  moe_status rc = allow_smem(moe_gate_up_kernel<SPW, NSEG, FULL, KH, MINB>, smem);
   if (rc != MOE_OK) return rc;
   const int groups = (s->top_k + SPW - 1) / SPW;
   const dim3 grid((unsigned)(B * groups), (unsigned)(s->I / kWarpsPerCta));
-  moe_gate_up_kernel<SPW, NSEG, FULL, KH><<<grid, kThreads, smem, st>>>(
+  moe_gate_up_kernel<SPW, NSEG, FULL, KH, MINB><<<grid, kThreads, smem, st>>>(
       w->gu_codes, w->gu_scales, x, ids, h, err, s->H, s->I, s->E, s->top_k, route);
   return MOE_OK;
 }
