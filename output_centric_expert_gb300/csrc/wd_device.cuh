@@ -108,8 +108,7 @@ moe_status launch_gate_up_kernels(const moe_shape* s, const moe_weights* w, cons
                                   cudaStream_t st, RouteArgs route);
 // moe_gate_up with a kernel compiled for the shape's H, if there is one:
 // returns false (launching nothing) otherwise. spw: routed slots per warp;
-// ctas_per_sm: 3, or 4 (64 registers; 2 or 4 slots per warp, H = 2048 or
-// 4096 only).
+// ctas_per_sm: 3, or 4 (64 registers; 2 or 4 slots per warp).
 bool launch_gate_up_fixed_h(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                             const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
                             cudaStream_t st, RouteArgs route, int spw, int ctas_per_sm,

@@ -19,8 +19,7 @@ bool launch_fixed(const moe_shape* s, const moe_weights* w, const uint16_t* x, c
   }
 }
 
-// The same at four CTAs per SM (64 registers), for up to 4 slots per warp and
-// the row lengths 2048 and 4096.
+// The same at four CTAs per SM (64 registers), for up to 4 slots per warp.
 template <int SPW>
 bool launch_fixed4(const moe_shape* s, const moe_weights* w, const uint16_t* x, const int32_t* ids,
                    int32_t B, uint16_t* h, int32_t* err, cudaStream_t st, RouteArgs route,
@@ -28,6 +27,7 @@ bool launch_fixed4(const moe_shape* s, const moe_weights* w, const uint16_t* x, 
   switch (s->H) {
     case 2048: *rc = launch_gate_up<SPW, 1, true, 2048, 4>(s, w, x, ids, B, h, err, st, route); return true;
     case 4096: *rc = launch_gate_up<SPW, 2, true, 4096, 4>(s, w, x, ids, B, h, err, st, route); return true;
+    case 7168: *rc = launch_gate_up<SPW, 4, false, 7168, 4>(s, w, x, ids, B, h, err, st, route); return true;
     default: return false;
   }
 }
