@@ -194,14 +194,15 @@ __global__ void __launch_bounds__(kThreads, (OPW * UPL >= 8) ? 2 : 3)
 }
 
 // Outputs per warp of moe_down beyond the single-wave small batches: 8 for
-// rows of at most 1024 elements (measured faster there from B=16 up: Q30
-// B=16 39.5 -> 31.1 us against 2 outputs per warp; slower for the 1536-element
-// rows of the 235B-shaped layer), else as many as keep at least kMinCtasPerSm
-// CTAs per SM.
+// rows of at most 1536 elements, else as many as keep at least kMinCtasPerSm
+// CTAs per SM. Measured on GB300 (in the layer, CUDA graph): Q30 B=16 39.5 ->
+// 31.1 us against 2 outputs per warp; Qwen-3-235B-A22B B=8 167.8 -> 154.4 us
+// against 2, even with 4 at 16 and 20 tokens; for the 2048-element rows of
+// the DeepSeek-V3 shape 8 was up to 0.7 % slower than 4 at 8-40 tokens.
 // A CTA covers 8 * OPW outputs, so OPW = 8 needs H % 64 == 0 (H % 32 == 0 is
 // enough for the others).
 int pick_opw(int B, int H, int I, int sms) {
-  if (H % (kWarpsPerCta * 8) == 0 && I <= 1024) return 8;
+  if (H % (kWarpsPerCta * 8) == 0 && I <= 1536) return 8;
   const int opws[3] = {4, 2, 1};
   for (int v : opws) {
     const int64_t ctas = (int64_t)B * (H / (kWarpsPerCta * v));
@@ -238,21 +239,18 @@ moe_status launch_down_ki(const moe_shape* s, const moe_weights* w, const uint16
 }
 
 // Row lengths with their own compiled kernel: the intermediate sizes of the
-// Qwen3-30B-A3B-, Qwen3-235B-A22B- and DeepSeek-V3-shaped layers (8 outputs
-// per warp is only chosen for I <= 1024); every other I runs the kernel that
-// reads I at run time.
+// Qwen3-30B-A3B-, Qwen3-235B-A22B- and DeepSeek-V3-shaped layers; every other
+// I runs the kernel that reads I at run time.
 template <int OPW, int UPL>
 moe_status launch_down(const moe_shape* s, const moe_weights* w, const uint16_t* h,
                        const int32_t* ids, const float* wts, int32_t B, float* y, int32_t* err,
                        cudaStream_t st, bool dependent, const float* logits) {
   if (s->I == 768)
     return launch_down_ki<OPW, UPL, 768>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
-  if constexpr (OPW != 8) {
-    if (s->I == 1536)
-      return launch_down_ki<OPW, UPL, 1536>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
-    if (s->I == 2048)
-      return launch_down_ki<OPW, UPL, 2048>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
-  }
+  if (s->I == 1536)
+    return launch_down_ki<OPW, UPL, 1536>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
+  if (s->I == 2048)
+    return launch_down_ki<OPW, UPL, 2048>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
   return launch_down_ki<OPW, UPL, 0>(s, w, h, ids, wts, B, y, err, st, dependent, logits);
 }
 
