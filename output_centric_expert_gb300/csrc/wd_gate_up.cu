@@ -69,22 +69,23 @@ moe_status launch_gate_up_kernels(const moe_shape* s, const moe_weights* w, cons
     spw = pick_spw(B, s->top_k, s->I);
     // Up to 1.5 E pairs, for the rows compiled with fixed length: four CTAs
     // per SM (64 registers) with 4 (slot, segment) units per warp (H = 2048;
-    // H = 4096 up to E pairs) or 8 (H = 4096 beyond E pairs; H = 7168).
-    // Measured on GB300 in the layer (CUDA graph, against 8 slots per warp at
-    // three CTAs per SM): Qwen-3-30B-A3B shape B=8..24 3-6 % faster (B=16
-    // 75.1 -> 70.9 us), slower from 28 tokens; Qwen-3-235B-A22B shape B=4..20
-    // 3-8 % faster (B=12 239.0 -> 221.1 us); DeepSeek-V3 shape B=4..40 2-12 %
-    // faster (B=32 1347.7 -> 1188.7 us). Each intermediate is the same bit
-    // for bit.
+    // H = 4096 up to E pairs or with top_k < 4) or 8 (H = 4096 beyond E
+    // pairs; H = 7168). Measured on GB300 in the layer (CUDA graph, against
+    // the slots per warp the CTA-count rule gives at three CTAs per SM):
+    // Qwen-3-30B-A3B shape B=8..24 3-6 % faster (B=16 75.1 -> 70.9 us),
+    // slower from 28 tokens; Qwen-3-235B-A22B shape B=4..20 3-8 % faster
+    // (B=12 239.0 -> 221.1 us); DeepSeek-V3 shape B=4..40 2-12 % faster (B=32
+    // 1347.7 -> 1188.7 us); Mixtral shape (top-2) B=2..5 2-5 % faster. Each
+    // intermediate is the same bit for bit.
     const int64_t P = (int64_t)B * s->top_k, E = s->E;
-    if (2 * P <= 3 * E && s->top_k >= 4) {
-      if (s->H == 2048) {
+    if (2 * P <= 3 * E) {
+      if (s->H == 2048 && s->top_k >= 4) {
         spw = 4;
         ctas_per_sm = 4;
-      } else if (s->H == 4096) {
-        spw = P <= E ? 2 : 4;
+      } else if (s->H == 4096 && s->top_k >= 2) {
+        spw = (P <= E || s->top_k < 4) ? 2 : 4;
         ctas_per_sm = 4;
-      } else if (s->H == 7168) {
+      } else if (s->H == 7168 && s->top_k >= 2) {
         spw = 2;
         ctas_per_sm = 4;
       }
