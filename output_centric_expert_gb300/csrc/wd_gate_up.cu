@@ -67,7 +67,9 @@ moe_status launch_gate_up_kernels(const moe_shape* s, const moe_weights* w, cons
   int spw = small_batch_spw(B, s->top_k, s->I, nseg), ctas_per_sm = 3;
   if (spw == 0) {
     spw = pick_spw(B, s->top_k, s->I);
-    // Up to 1.5 E pairs, for the rows compiled with fixed length: four CTAs
+    // Below the grouped switch (1.5 E pairs for H = 2048, where 8 slots at
+    // three CTAs win from 28 tokens; 1.625 E pairs from H = 4096), for the
+    // rows compiled with fixed length: four CTAs
     // per SM (64 registers) with 4 (slot, segment) units per warp (H = 2048;
     // H = 4096 up to E pairs or with top_k < 4) or 8 (H = 4096 beyond E
     // pairs; H = 7168). Measured on GB300 in the layer (CUDA graph, against
@@ -78,7 +80,7 @@ moe_status launch_gate_up_kernels(const moe_shape* s, const moe_weights* w, cons
     // 1347.7 -> 1188.7 us); Mixtral shape (top-2) B=2..5 2-5 % faster. Each
     // intermediate is the same bit for bit.
     const int64_t P = (int64_t)B * s->top_k, E = s->E;
-    if (2 * P <= 3 * E) {
+    if (s->H == 2048 ? 2 * P <= 3 * E : 8 * P < 13 * E) {
       if (s->H == 2048 && s->top_k >= 4) {
         spw = 4;
         ctas_per_sm = 4;

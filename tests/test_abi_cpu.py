@@ -206,7 +206,7 @@ def test_layer_gate_up_kernel_rule():
         sh = ops.make_shape(H, I, E, k)
         for B in (1, 2, 5, 16, 17, 39, 40, 64, 65, 256):
             P = B * k
-            shared = (2 * P >= 3 * E) if H >= 4096 else (2 * P >= 5 * E)
+            shared = (8 * P >= 13 * E) if H >= 4096 else (2 * P >= 5 * E)
             want = "grouped" if (shared and H % 256 == 0 and I % 64 == 0 and E <= 256) else "per_token"
             assert ops.layer_gate_up_kernel(sh, B) == want, (H, I, E, k, B)
     # misaligned scales keep the per-token kernel; a bad shape is an error
@@ -251,10 +251,13 @@ def test_layer_host_kernel_choice():
     ids12 = ids13[:12]
     assert ops.layer_host_kernels(sh1, ids13) == ("grouped", "grouped")
     assert ops.layer_host_kernels(sh1, ids12) == ("per_token", "per_token")
-    # longer rows: gate/up from 1.75 pairs per expert (H >= 4096), down from 2.2 (H >= 6144)
+    # longer rows: gate/up from 1.95 pairs per expert (H >= 4096), down from 2.2 (H >= 6144)
     sh4 = ops.make_shape(4096, 1536, 128, 1)
     ids9 = np.array([[e] for e in [0, 1, 2, 3] * 2 + [0]], dtype=np.int32)  # 9 on 4: 2.25
     assert ops.layer_host_kernels(sh4, ids9) == ("grouped", "per_token")
+    ids39 = np.array([[e] for e in list(range(20)) + list(range(19))], dtype=np.int32)  # 39 on 20
+    assert ops.layer_host_kernels(sh4, ids39)[0] == "grouped"  # 1.95 pairs per used expert
+    assert ops.layer_host_kernels(sh4, ids39[:38])[0] == "per_token"  # 1.9
     sh7 = ops.make_shape(7168, 2048, 256, 1)
     assert ops.layer_host_kernels(sh7, ids9) == ("grouped", "grouped")
     assert ops.layer_host_kernels(sh7, ids9[:8]) == ("grouped", "per_token")  # 2.0 per expert
