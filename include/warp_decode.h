@@ -26,13 +26,13 @@
  * LAYER KERNEL CHOICE (moe_layer, moe_layer_noalloc, moe_layer_routed with
  * ids_out), with P = B * top_k routed pairs, measured on GB300 under uniform
  * routing:
- *   gate/up grouped when 2P >= 5E (H < 4096), 8P >= 13E (H >= 4096);
+ *   gate/up grouped when P >= 2E (H < 4096), 8P >= 13E (H >= 4096);
  *   down grouped when    2P >= 5E (H < 6144), P >= 2E (H >= 6144);
  * each only where the grouped kernel takes the shape and batch. The choice
  * is reported by moe_layer_gate_up_kernel and moe_layer_down_kernel.
  * moe_layer_host has the ids on the host and counts the batch's distinct
  * valid experts U instead (E <= 256):
- *   gate/up grouped when P >= 2.6 U (H < 4096), P >= 1.95 U (H >= 4096);
+ *   gate/up grouped when P >= 2.15 U (H < 4096), P >= 1.95 U (H >= 4096);
  *   down grouped when    P >= 2.6 U (H < 6144), P >= 2.2 U (H >= 6144);
  * the same break-even points under uniform routing, and earlier where the
  * pairs crowd onto few experts (skewed routing); moe_layer_host_kernels

@@ -154,8 +154,10 @@ moe_status gate_up_impl(const moe_shape* s, const moe_weights* w, const uint16_t
 // once the batch has enough pairs per expert, if the shape allows it. The
 // switch points are measured on GB300 in the layer (CUDA graph, cold L2,
 // uniform routing), with the per-token kernel at its four-CTA launch where
-// that applies: per-token vs grouped gate/up break even at about 36 tokens
-// for the Qwen-3-30B-A3B shape (2.25 E pairs; H = 2048), 25 for the
+// that applies and the grouped one at one column tile: per-token vs grouped
+// gate/up break even at about 30 tokens for the Qwen-3-30B-A3B shape (1.9 E
+// pairs; H = 2048: layer at 28 tokens 104.5 us per-token vs 109.7 with the
+// grouped gate/up, at 32 tokens 117.9 vs 116.3, at 36 128.2 vs 121.2), 25 for the
 // Qwen-3-235B-A22B shape (1.6 E; H = 4096: 24 tokens 354.9 us per-token vs
 // 361.1 grouped, 28 tokens 410.5 vs 380.9) and 52 for the DeepSeek-V3 shape
 // (1.6 E; H = 7168: 48 tokens 1655 vs 1850, 56 tokens 2097 vs 1999). The
@@ -164,7 +166,7 @@ GateUpForm layer_form(const moe_shape* s, const moe_weights* w, int32_t B) {
   if (!s) return GateUpForm::kPerToken;
   const int64_t pairs = (int64_t)B * s->top_k, E = s->E;
   const bool shared = s->H >= 4096 ? 8 * pairs >= 13 * E  // 1.625 E pairs
-                                   : 2 * pairs >= 5 * E;  // 2.5 E
+                                   : pairs >= 2 * E;      // 2 E
   if (shared && gate_up_grouped_supported(s, w, B)) return GateUpForm::kGrouped;
   return GateUpForm::kPerToken;
 }
@@ -220,9 +222,9 @@ DownForm layer_down_form(const moe_shape* s, const moe_weights* w, int32_t B) {
 // distinct experts of the batch, so that a batch whose pairs crowd onto few
 // experts (skewed routing) takes the grouped kernels where they win. With
 // uniform routing U = E (1 - (1 - k/E)^B) on average, and the thresholds
-// reproduce the rules on P and E at the measured shapes: gate/up tau = 2.6
-// (H < 4096; Qwen-3-30B-A3B: 2.49 pairs per used expert at its 36-token
-// break-even, 2.71 at 40 tokens) or 1.95 (H >= 4096; Qwen-3-235B-A22B 1.90
+// reproduce the rules on P and E at the measured shapes: gate/up tau = 2.15
+// (H < 4096; Qwen-3-30B-A3B: 2.00-2.13 pairs per used expert at 28 tokens,
+// 2.19-2.39 at 32) or 1.95 (H >= 4096; Qwen-3-235B-A22B 1.90
 // at 24 tokens and 2.0 at 26, DeepSeek-V3 shape 1.92 at 48 and 2.01 at 52,
 // Mixtral shape 1.82 at 6 and 2.02 at 7); down
 // tau = 2.6 (H < 6144) or 2.2 (H >= 6144; DeepSeek-V3 shape 2.1 at 55
@@ -251,7 +253,7 @@ LayerForms layer_forms_for_ids(const moe_shape* s, const moe_weights* w, const i
     }
   }
   if (U == 0) return f;
-  const bool gu_shared = s->H >= 4096 ? 20 * P >= 39 * U : 5 * P >= 13 * U;
+  const bool gu_shared = s->H >= 4096 ? 20 * P >= 39 * U : 20 * P >= 43 * U;
   const bool dn_shared = s->H >= 6144 ? 5 * P >= 11 * U : 5 * P >= 13 * U;
   if (gu_shared && gate_up_grouped_supported(s, w, B)) f.gate_up = GateUpForm::kGrouped;
   if (dn_shared && down_grouped_supported(s, w, B)) f.down = DownForm::kGrouped;

@@ -190,23 +190,23 @@ def test_header_is_plain_c_and_links(tmp_path):
 
 def test_layer_gate_up_kernel_rule():
     """The library's statement of the layer's gate/up kernel (a host-only call):
-    the grouped kernel from 2*B*top_k >= 5E when it takes the shape (H % 256,
-    I % 64), the per-token kernel otherwise. The GPU test
-    test_layer_uses_the_grouped_kernel_from_2_5e_pairs checks that the layer
-    really runs the kernel reported here."""
+    the grouped kernel from B*top_k >= 2E (H < 4096) or 8*B*top_k >= 13E
+    (H >= 4096) when it takes the shape (H % 256, I % 64), the per-token kernel
+    otherwise. The GPU test test_layer_uses_the_grouped_kernel_from_2e_pairs
+    checks that the layer really runs the kernel reported here."""
     q30 = ops.make_shape(2048, 768, 128, 8)
-    assert ops.layer_gate_up_kernel(q30, 39) == "per_token"
-    assert ops.layer_gate_up_kernel(q30, 40) == "grouped"
+    assert ops.layer_gate_up_kernel(q30, 31) == "per_token"
+    assert ops.layer_gate_up_kernel(q30, 32) == "grouped"
     assert ops.layer_gate_up_kernel(ops.make_shape(2080, 768, 128, 8), 64) == "per_token"
     assert ops.layer_gate_up_kernel(ops.make_shape(2048, 96, 128, 8), 64) == "per_token"
-    assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 9) == "per_token"
-    assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 10) == "grouped"
+    assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 7) == "per_token"
+    assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 8) == "grouped"
     for (H, I, E, k) in [(2048, 768, 128, 8), (4096, 1536, 128, 8), (7168, 2048, 256, 8),
                          (4096, 14336, 8, 2), (256, 128, 8, 2), (768, 192, 5, 3)]:
         sh = ops.make_shape(H, I, E, k)
-        for B in (1, 2, 5, 16, 17, 39, 40, 64, 65, 256):
+        for B in (1, 2, 5, 7, 8, 16, 17, 31, 32, 39, 40, 64, 65, 256):
             P = B * k
-            shared = (8 * P >= 13 * E) if H >= 4096 else (2 * P >= 5 * E)
+            shared = (8 * P >= 13 * E) if H >= 4096 else (P >= 2 * E)
             want = "grouped" if (shared and H % 256 == 0 and I % 64 == 0 and E <= 256) else "per_token"
             assert ops.layer_gate_up_kernel(sh, B) == want, (H, I, E, k, B)
     # misaligned scales keep the per-token kernel; a bad shape is an error
@@ -221,16 +221,21 @@ def test_layer_gate_up_kernel_rule():
 def test_layer_host_kernel_choice():
     """moe_layer_host picks its kernels from the batch's own ids: pairs per used
     expert against the measured break-even points. Uniform routing gives the
-    same choice as the rules on B (Qwen-3-30B-A3B shape: per-token at 32 tokens,
-    grouped from 40); a skewed batch of 32 tokens, its pairs on a few dozen
+    same choice as the rules on B (Qwen-3-30B-A3B shape: per-token at 16 tokens,
+    grouped gate/up from 32, both grouped from 40); a skewed batch of 32 tokens,
+    its pairs on a few dozen
     experts, takes the grouped kernels; all on one expert likewise; no valid id
     keeps the per-token kernels. Host-only."""
     from output_centric_expert_gb300 import workload
     q30 = workload.SHAPES["q30"]
     sh = ops.make_shape(q30.H, q30.I, q30.E, q30.top_k)
-    for B in (8, 16, 32, 36):
+    for B in (8, 16, 28):  # 28 tokens: 2.13 pairs per used expert
         ids = workload.tokens(q30, B, seed=0, batch=0, routing="uniform")[1]
         assert ops.layer_host_kernels(sh, ids) == ("per_token", "per_token"), B
+    for B in (32, 36):  # 2.29 and 2.46 pairs per used expert
+        ids = workload.tokens(q30, B, seed=0, batch=0, routing="uniform")[1]
+        assert ops.layer_host_kernels(sh, ids) == ("grouped", "per_token"), B
+        assert ops.layer_gate_up_kernel(sh, B) == "grouped" and ops.layer_down_kernel(sh, B) == "per_token"
     for B in (40, 48, 64):
         ids = workload.tokens(q30, B, seed=0, batch=0, routing="uniform")[1]
         assert ops.layer_host_kernels(sh, ids) == ("grouped", "grouped"), B
@@ -244,13 +249,17 @@ def test_layer_host_kernel_choice():
     assert ops.layer_host_kernels(sh, one) == ("grouped", "grouped")
     none = np.full((8, 8), -1, dtype=np.int32)
     assert ops.layer_host_kernels(sh, none) == ("per_token", "per_token")
-    # the thresholds in pairs per used expert, at a boundary: 13 pairs on 5 experts
-    # is 2.6 per expert (grouped), 12 on 5 is 2.4 (per-token); top_k = 1
+    # the thresholds in pairs per used expert, at a boundary (top_k = 1): down
+    # grouped from 2.6 per expert (13 pairs on 5 experts; 12 on 5 is 2.4), gate/up
+    # from 2.15 (43 pairs on 20 experts; 42 on 20 is 2.1)
     sh1 = ops.make_shape(2048, 768, 128, 1)
     ids13 = np.array([[e] for e in [0, 1, 2, 3, 4] * 2 + [0, 1, 2]], dtype=np.int32)
     ids12 = ids13[:12]
     assert ops.layer_host_kernels(sh1, ids13) == ("grouped", "grouped")
-    assert ops.layer_host_kernels(sh1, ids12) == ("per_token", "per_token")
+    assert ops.layer_host_kernels(sh1, ids12) == ("grouped", "per_token")
+    ids43 = np.array([[e] for e in list(range(20)) * 2 + [0, 1, 2]], dtype=np.int32)
+    assert ops.layer_host_kernels(sh1, ids43) == ("grouped", "per_token")
+    assert ops.layer_host_kernels(sh1, ids43[:42]) == ("per_token", "per_token")
     # longer rows: gate/up from 1.95 pairs per expert (H >= 4096), down from 2.2 (H >= 6144)
     sh4 = ops.make_shape(4096, 1536, 128, 1)
     ids9 = np.array([[e] for e in [0, 1, 2, 3] * 2 + [0]], dtype=np.int32)  # 9 on 4: 2.25

@@ -118,8 +118,8 @@ def test_layer_switches_down_kernel_at_2_5e_pairs(q30):
                                              (32, "uniform", 0), (40, "uniform", 2)])
 def test_host_entry_point_chooses_from_its_ids(q30, B, routing, batch):
     """moe_layer_host picks its kernels from the batch's own ids (pairs per used
-    expert): a skewed batch of 32 tokens runs the grouped kernels although
-    moe_layer, which decides on B, runs the per-token ones there. Its y equals,
+    expert): a skewed batch of 32 tokens runs both grouped kernels although
+    moe_layer, which decides on B, runs the per-token down kernel there. Its y equals,
     bit for bit, the kernels it reports run one after the other on the same
     device inputs, and the oracle on sampled tokens."""
     x, ids, w = workload.tokens(q30.shape, B, routing=routing, batch=batch)

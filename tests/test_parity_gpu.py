@@ -293,10 +293,10 @@ def test_batch_equals_tokens_one_at_a_time(request, form, which, B, routing):
         assert np.array_equal(y1[0], y[t]), t
 
 
-def test_layer_uses_the_grouped_kernel_from_2_5e_pairs(q30):
-    """moe_layer's intermediate equals moe_gate_up's below 2*B*top_k = 5E and
-    moe_gate_up_grouped's from there on (Qwen-3-30B-A3B shape: 40 tokens)."""
-    for B in (39, 40):
+def test_layer_uses_the_grouped_kernel_from_2e_pairs(q30):
+    """moe_layer's intermediate equals moe_gate_up's below B*top_k = 2E and
+    moe_gate_up_grouped's from there on (Qwen-3-30B-A3B shape: 32 tokens)."""
+    for B in (31, 32):
         x, ids, w = workload.tokens(q30.shape, B, batch=700 + B)
         _, h = _run_layer(q30, x, ids, w)
         hp = torch.empty((B, 8, q30.shape.I), dtype=torch.int16, device="cuda")
@@ -304,7 +304,8 @@ def test_layer_uses_the_grouped_kernel_from_2_5e_pairs(q30):
         ops.moe_gate_up(q30.dev, _dev(x.view(np.int16)), _dev(ids), hp)
         ops.moe_gate_up_grouped(q30.dev, _dev(x.view(np.int16)), _dev(ids), hg)
         torch.cuda.synchronize()
-        want = (hg if 2 * B * 8 >= 5 * 128 else hp).cpu().numpy().view(np.uint16)
+        assert ops.layer_gate_up_kernel(q30.sh, B) == ("grouped" if B * 8 >= 2 * 128 else "per_token")
+        want = (hg if B * 8 >= 2 * 128 else hp).cpu().numpy().view(np.uint16)
         assert np.array_equal(h, want), B
 
 
