@@ -16,13 +16,15 @@
 //   the warp's 8 neurons, rows 8-15 their up rows, so a lane's accumulator
 //   fragment holds gate and up of one neuron for two pairs and the SwiGLU
 //   epilogue needs no exchange between lanes. The 8 columns are 8 of the
-//   expert's routed pairs (two column tiles per pass where shared memory
-//   allows, and several passes over the rows when more pairs are routed).
+//   expert's routed pairs (several passes over the rows when more pairs are
+//   routed).
 //
 // Reduction order. The contraction over H runs block by block: within one
 // 32-element MXFP8 block the two MMAs sum the exact f16 x E4M3 products in
 // FP32 (the tensor core's own order), the block sum is multiplied by the
-// block's E8M0 scale and added to an FP32 accumulator. The k axis inside a
+// block's E8M0 scale and added to an FP32 accumulator; the blocks of the
+// lower half of H and those of the upper half go to two accumulators, added
+// at the end (lower + upper), however the item is run. The k axis inside a
 // block is permuted identically for both operands: a quad of lanes loads 64
 // contiguous codes (two blocks, 16 codes per lane), the lanes q and q^2 swap
 // their upper 8 codes, and then lane q holds 8 codes of each block, at
@@ -33,8 +35,15 @@
 //
 // Work. A persistent grid of two CTAs per SM. Every CTA lists the batch's
 // pairs by expert in pair order and numbers the work items (expert, pass of
-// up to 16 pairs, 64-neuron tile) with the items of one (expert, pass)
-// consecutive; CTA c takes the c-th contiguous share. For each new (expert,
+// up to 8 pairs, 64-neuron tile) with the items of one (expert, pass)
+// consecutive; CTA c takes the c-th contiguous share, counted in half-items
+// of 32 neurons where that lowers the largest share. A half-item without its
+// partner in the share runs on all 8 warps, each half of H on 4 of them, and
+// the two partial sums meet in shared memory: at 4.5 items per CTA (the
+// Qwen-3-30B-A3B shape at 32 tokens) the CTAs with 5 whole items left the
+// others idle for a fifth of the kernel (74.0 -> 69.0 us; 64 tokens 83.5 ->
+// 79.7, skewed 32 tokens 45.6 -> 41.9, Qwen-3-235B-A22B 64 tokens 281.3 ->
+// 269.4, Mixtral-shaped 8 tokens 147.0 -> 138.0). For each new (expert,
 // pass) the CTA stages its pairs' activations in shared memory as the same
 // f16 x 2^sigma copy of the BF16 row as the per-token kernel (sigma per
 // token) and keeps them for the pass's following tiles. Codes stream through
@@ -50,10 +59,10 @@
 // bytes per lane (32 bytes per row) the L1 data pipe was the busiest unit
 // (about 60 % of peak against 47 % for DRAM, ncu, Qwen-3-30B-A3B shape at 32
 // tokens); 16 bytes per lane and the swap cut the kernel's time there from
-// 95.5 to 83.7 us with bit-identical results. Measured on GB300 it is faster
-// than the per-token kernel from about 36 tokens (Qwen-3-30B-A3B shape) or
-// 17 tokens (Qwen-3-235B-A22B shape) under uniform routing, and at 32 tokens
-// under skewed routing.
+// 95.5 to 83.7 us with bit-identical results. Measured on GB300, in the
+// layer, it is faster than the per-token kernel from about 30 tokens
+// (Qwen-3-30B-A3B shape) or 25 tokens (Qwen-3-235B-A22B shape) under uniform
+// routing, and far ahead at 32 skewed tokens.
 #include "wd_device.cuh"
 #include "wd_gate_up_grouped.h"
 
@@ -70,7 +79,7 @@ constexpr int kGrpCols = 8;                                      // pairs per MM
 __host__ __device__ constexpr int grp_row_bytes(int H) { return 2 * H + 64; }
 
 // UNR: 32-element blocks per loop step (a multiple of 8: one 64-bit load of
-// scales per row per 8 blocks). NCH: column tiles of 8 pairs held at once.
+// scales per row per 8 blocks).
 template <int UNR>
 struct GrpBuf {
   uint4 g[UNR / 2], u[UNR / 2];    // this lane's 16 codes of each block pair, gate and up
@@ -82,11 +91,11 @@ struct GrpLayout {
   size_t xs, list, cnt, start, istart, run, wc, total;
 };
 
-__host__ __device__ inline GrpLayout grp_layout(int H, int E, int P, int kT) {
+__host__ __device__ inline GrpLayout grp_layout(int H, int E, int P) {
   GrpLayout L;
   size_t o = 0;
-  L.xs = o;      // [kT] staged activation rows of grp_row_bytes(H)
-  o += (size_t)kT * grp_row_bytes(H);
+  L.xs = o;      // [kGrpCols] staged activation rows of grp_row_bytes(H)
+  o += (size_t)kGrpCols * grp_row_bytes(H);
   L.list = o;    // [P] int: pair indices grouped by expert, in pair order
   o += (size_t)P * 4;
   L.cnt = o;     // [E] int: pairs routed to each expert
@@ -97,8 +106,9 @@ __host__ __device__ inline GrpLayout grp_layout(int H, int E, int P, int kT) {
   o += (size_t)(E + 1) * 4;
   L.run = o;     // [E] int: entries placed so far
   o += (size_t)E * 4;
-  L.wc = o;      // [warp][E] int: per-warp counts while placing
-  o += (size_t)kWarpsPerCta * E * 4;
+  L.wc = o;      // [warp][E] int: per-warp counts while placing; afterwards the
+                 // upper-half partial sums of a split half-item, [4 warps][32 lanes][4] float
+  o += (size_t)(kWarpsPerCta * E > 4 * 32 * 4 ? kWarpsPerCta * E : 4 * 32 * 4) * 4;
   L.total = o;
   return L;
 }
@@ -106,10 +116,11 @@ __host__ __device__ inline GrpLayout grp_layout(int H, int E, int P, int kT) {
 // Persistent: a grid of two CTAs per SM. Every CTA lists the batch's pairs by
 // expert (in pair order) and numbers the work items (expert, pass of kT pairs,
 // 64-neuron tile), items of one (expert, pass) consecutive; CTA c takes the
-// c-th contiguous share of the items. The staged activations of a pass serve
-// all of its tiles that fall to the CTA, and each warp requests the first
-// codes of its next item while it computes the last ones of the current item.
-template <int UNR, int NCH>
+// c-th contiguous share of the items or half-items. The staged activations of
+// a pass serve all of its tiles that fall to the CTA, and each warp requests
+// the first codes of its next unit while it computes the last ones of the
+// current unit.
+template <int UNR>
 __global__ void __launch_bounds__(kThreads, 2)
     moe_gate_up_grouped_kernel(const uint8_t* __restrict__ gu_codes,
                                const uint8_t* __restrict__ gu_scales,
@@ -117,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                                uint16_t* __restrict__ h, int32_t* __restrict__ err, int H, int I,
                                int E, int top_k, int B) {
   static_assert(UNR % 8 == 0, "UNR: multiple of 8");
-  constexpr int kT = NCH * kGrpCols;  // pairs staged per pass
+  constexpr int kT = kGrpCols;  // pairs staged per pass
   constexpr unsigned kFull = 0xFFFFFFFFu;
   extern __shared__ uint4 dyn4[];
   __shared__ int s_pair[kT];          // pair index t*top_k + j of each staged column
@@ -125,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ int s_wtot[2][kWarpsPerCta];
 
   const int P = B * top_k;
-  const GrpLayout L = grp_layout(H, E, P, kT);
+  const GrpLayout L = grp_layout(H, E, P);
   uint8_t* dsm = reinterpret_cast<uint8_t*>(dyn4);
   uint8_t* xs = dsm + L.xs;
   int* s_list = reinterpret_cast<int*>(dsm + L.list);
@@ -223,13 +234,46 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
 
+  // Work units. A half-item is 32 of an item's 64 neurons, and CTA c takes the
+  // c-th contiguous share of the 2 * nitems half-items, so that the shares
+  // differ by at most one half-item. Two half-items of one item run as the
+  // whole item (warp w: neurons 8w .. 8w+7 over all of H); a half-item whose
+  // partner is outside the share runs alone on all 8 warps, warps w and w+4
+  // taking neurons 8(w&3) .. of it over the lower and the upper half of H,
+  // and the two partial sums are added in shared memory. Every item sums the
+  // lower and the upper half of H separately and adds the two at the end,
+  // whichever way it runs, so a result does not depend on how the batch fell
+  // into shares. (Rows of one 8-block group: whole items only.)
+  static_assert(kWarpsPerCta == 8, "a split half-item pairs warps w and w + 4");
   const int nitems = s_istart[E];
-  const int i0 = (int)((int64_t)nitems * blockIdx.x / gridDim.x);
-  const int i1 = (int)((int64_t)nitems * (blockIdx.x + 1) / gridDim.x);
-  if (i0 >= i1) return;  // the same for every thread of the CTA
+  const int nit = nblk / UNR;
+  const int half = nit >= 2 ? nit / 2 : nit;  // groups summed into the lower partial
+  // shares in half-items where that lowers the largest share (an odd number
+  // of half-items at most per CTA); else in whole items, which run no split
+  const bool halves =
+      nit >= 2 && ((2 * (int64_t)nitems + gridDim.x - 1) / gridDim.x) % 2 == 1;
+  const int64_t nunits = halves ? 2 * (int64_t)nitems : (int64_t)nitems;
+  const int u0 = (int)(nunits * blockIdx.x / gridDim.x);
+  const int u1 = (int)(nunits * (blockIdx.x + 1) / gridDim.x);
+  if (u0 >= u1) return;  // the same for every thread of the CTA
 
-  auto load = [&](int e_, int tile_, int it, GrpBuf<UNR>& U) {
-    const size_t row = (size_t)e_ * I + tile_ * kGrpNeurons + warp * kGrpNeuronsPerWarp + g;
+  auto is_single = [&](int u) { return halves && ((u & 1) || u + 1 >= u1); };
+  auto item_of = [&](int u) { return halves ? (u >> 1) : u; };
+  // this warp's first neuron and its groups [gb, ge) of 8 blocks in a unit
+  auto role = [&](int tile_, bool single, int hsel, int& nbase, int& gb, int& ge) {
+    if (!single) {
+      nbase = tile_ * kGrpNeurons + warp * kGrpNeuronsPerWarp;
+      gb = 0;
+      ge = nit;
+    } else {
+      nbase = tile_ * kGrpNeurons + hsel * (kGrpNeurons / 2) + (warp & 3) * kGrpNeuronsPerWarp;
+      gb = warp < 4 ? 0 : half;
+      ge = warp < 4 ? half : nit;
+    }
+  };
+
+  auto load = [&](int e_, int nbase_, int it, GrpBuf<UNR>& U) {
+    const size_t row = (size_t)e_ * I + nbase_ + g;
     const uint8_t* grow = gu_codes + row * 2 * H + q * 16;  // gate row, this lane's 16 B
     const uint8_t* urow = grow + H;
     const uint8_t* gsc = gu_scales + row * 2 * nblk;
@@ -252,10 +296,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   const bool low = q < 2;
   const uint8_t* xl = xs + g * RS;  // column g of tile 0
   const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float* comb = reinterpret_cast<float*>(dsm + L.wc);  // free once the pairs are placed
 
   // the expert of item i: the last expert whose first item is at most i
   int e = 0;
   {
+    const int i0 = item_of(u0);
     int lo = 0, hi = E - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -264,18 +310,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     e = lo;
   }
-  const int nit = nblk / UNR;
-  GrpBuf<UNR> U0, U1;
-  load(e, (i0 - s_istart[e]) % tiles, 0, U0);  // the first codes, before any staging
-  int staged_e = -1, staged_pass = -1;
-
   // the expert of item i, searched on from expert e
   auto expert_after = [&](int i, int e_) {
     while (e_ + 1 < E && s_istart[e_ + 1] <= i) ++e_;
     return e_;
   };
-  for (int i = i0; i < i1; ++i) {
-    const int rem = i - s_istart[e];
+  GrpBuf<UNR> U0, U1;
+  {  // the first codes, before any staging
+    int nb, gb, ge;
+    role((item_of(u0) - s_istart[e]) % tiles, is_single(u0), u0 & 1, nb, gb, ge);
+    load(e, nb, gb, U0);
+  }
+  int staged_e = -1, staged_pass = -1;
+
+  for (int u = u0; u < u1;) {
+    const bool single = is_single(u);
+    const int rem = item_of(u) - s_istart[e];
     const int pass = rem / tiles, tile = rem - pass * tiles;
 
     const int cols = min(kT, s_cnt[e] - pass * kT);
@@ -301,11 +351,22 @@ __global__ void __launch_bounds__(kThreads, 2)
       staged_e = e;
       staged_pass = pass;
     }
-    const int nch = (cols + kGrpCols - 1) / kGrpCols;
+    int nbase, gb, ge;
+    role(tile, single, u & 1, nbase, gb, ge);
+    const int un = u + ((halves && !single) ? 2 : 1);  // the next unit
 
-    float accg[NCH][2], accu[NCH][2];
+    // acc*: the running sum; lo*: the lower half of H's, once the upper half begins
+    float accg[2], accu[2], lowg[2], lowu[2];
 #pragma unroll
-    for (int c = 0; c < NCH; ++c) accg[c][0] = accg[c][1] = accu[c][0] = accu[c][1] = 0.0f;
+    for (int k = 0; k < 2; ++k) accg[k] = accu[k] = lowg[k] = lowu[k] = 0.0f;
+    auto stash = [&]() {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        lowg[k] = accg[k];
+        lowu[k] = accu[k];
+        accg[k] = accu[k] = 0.0f;
+      }
+    };
 
     auto compute = [&](int it, const GrpBuf<UNR>& U) {
 #pragma unroll
@@ -333,37 +394,36 @@ __global__ void __launch_bounds__(kThreads, 2)
           float sg, su;
           e8m0x2_to_f32(swd >> (8 * (ib % 4)), uwd >> (8 * (ib % 4)), sg, su);
           const int off = hb ? off_odd : off_even;
-#pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            if (c < nch) {
-              const uint4 xv = *reinterpret_cast<const uint4*>(
-                  xl + (size_t)c * kGrpCols * RS + b * 64 + 2 * off);
-              float d[4];
-              mma_16816(d, a0, xv.x, xv.y, zero);
-              mma_16816(d, a1, xv.z, xv.w, d);
-              accg[c][0] = fmaf(d[0], sg, accg[c][0]);
-              accg[c][1] = fmaf(d[1], sg, accg[c][1]);
-              accu[c][0] = fmaf(d[2], su, accu[c][0]);
-              accu[c][1] = fmaf(d[3], su, accu[c][1]);
-            }
-          }
+          const uint4 xv = *reinterpret_cast<const uint4*>(xl + b * 64 + 2 * off);
+          float d[4];
+          mma_16816(d, a0, xv.x, xv.y, zero);
+          mma_16816(d, a1, xv.z, xv.w, d);
+          accg[0] = fmaf(d[0], sg, accg[0]);
+          accg[1] = fmaf(d[1], sg, accg[1]);
+          accu[0] = fmaf(d[2], su, accu[0]);
+          accu[1] = fmaf(d[3], su, accu[1]);
         }
       }
     };
 
-    // the next item's first codes, into U0 once U0 is free
+    // the next unit's first codes for this warp, into U0 once U0 is free
     auto load_next = [&]() {
-      if (i + 1 < i1) {
-        const int en = expert_after(i + 1, e);
-        load(en, (i + 1 - s_istart[en]) % tiles, 0, U0);
+      if (un < u1) {
+        const int ni = item_of(un);
+        const int en = expert_after(ni, e);
+        int nb, b0, b1;
+        role((ni - s_istart[en]) % tiles, is_single(un), un & 1, nb, b0, b1);
+        load(en, nb, b0, U0);
       }
     };
-    for (int it = 0; it < nit; it += 2) {
-      if (it + 1 < nit) {
-        load(e, tile, it + 1, U1);
+    for (int it = gb; it < ge; it += 2) {
+      if (it == half) stash();
+      if (it + 1 < ge) {
+        load(e, nbase, it + 1, U1);
         compute(it, U0);
-        if (it + 2 < nit) load(e, tile, it + 2, U0);
+        if (it + 2 < ge) load(e, nbase, it + 2, U0);
         else load_next();
+        if (it + 1 == half) stash();
         compute(it + 1, U1);
       } else {  // an odd number of groups: the last one is in U0
         compute(it, U0);
@@ -371,35 +431,62 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
 
-    // Epilogue: lane (g, q) holds gate and up of neuron n for columns 2q, 2q+1.
-    const int n = tile * kGrpNeurons + warp * kGrpNeuronsPerWarp + g;
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
+    // The totals: lower partial + upper partial. A split half-item's upper
+    // partials come from warps 4-7 through shared memory.
+    bool writer = true;
+    if (single) {
+      float* cw = comb + ((warp & 3) * 32 + lane) * 4;
+      if (warp >= 4) {
+        cw[0] = accg[0];
+        cw[1] = accg[1];
+        cw[2] = accu[0];
+        cw[3] = accu[1];
+      }
+      __syncthreads();
+      writer = warp < 4;
+      if (writer) {
+        accg[0] += cw[0];
+        accg[1] += cw[1];
+        accu[0] += cw[2];
+        accu[1] += cw[3];
+      }
+    } else {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const int li = c * kGrpCols + 2 * q + k;
+        accg[k] = lowg[k] + accg[k];
+        accu[k] = lowu[k] + accu[k];
+      }
+    }
+    // Epilogue: lane (g, q) holds gate and up of neuron n for columns 2q, 2q+1.
+    if (writer) {
+      const int n = nbase + g;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int li = 2 * q + k;
         if (li < cols) {
           const float unscale = exp2i(-s_sig[li]);
-          const float gv = accg[c][k] * unscale, uv = accu[c][k] * unscale;
+          const float gv = accg[k] * unscale, uv = accu[k] * unscale;
           const float sl = gv / (1.0f + expf(-gv));
           const __nv_bfloat16 hv = __float2bfloat16_rn(sl * uv);
           h[(size_t)s_pair[li] * I + n] = *reinterpret_cast<const uint16_t*>(&hv);
         }
       }
     }
-    e = expert_after(i + 1, e);
+    if (single) __syncthreads();  // the combine buffer is free again
+    if (un < u1) e = expert_after(item_of(un), e);
+    u = un;
   }
 }
 
-template <int UNR, int NCH>
+template <int UNR>
 moe_status launch_grouped(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                           const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
                           cudaStream_t st) {
-  const size_t smem = grp_layout(s->H, s->E, B * s->top_k, NCH * kGrpCols).total;
-  moe_status rc = allow_smem(moe_gate_up_grouped_kernel<UNR, NCH>, smem);
+  const size_t smem = grp_layout(s->H, s->E, B * s->top_k).total;
+  moe_status rc = allow_smem(moe_gate_up_grouped_kernel<UNR>, smem);
   if (rc != MOE_OK) return rc;
   const unsigned grid = (unsigned)(2 * sm_count());
-  moe_gate_up_grouped_kernel<UNR, NCH><<<grid, kThreads, smem, st>>>(
+  moe_gate_up_grouped_kernel<UNR><<<grid, kThreads, smem, st>>>(
       w->gu_codes, w->gu_scales, x, ids, h, err, s->H, s->I, s->E, s->top_k, B);
   return MOE_OK;
 }
@@ -409,25 +496,21 @@ constexpr int kGrpUnroll = 8;
 }  // namespace
 
 bool gate_up_grouped_supported(const moe_shape* s, const moe_weights* w, int32_t B) {
-  // one pass of kGrpCols pairs at least; the larger of the two layouts
   return s->H % (32 * kGrpUnroll) == 0 && s->I % kGrpNeurons == 0 && s->E <= kThreads &&
          (w == nullptr || aligned(w->gu_scales, 8)) &&
-         grp_layout(s->H, s->E, B * s->top_k, kGrpCols).total <= kMaxDynSmem;
+         grp_layout(s->H, s->E, B * s->top_k).total <= kMaxDynSmem;
 }
 
 moe_status launch_gate_up_grouped(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                                   const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
                                   cudaStream_t st) {
-  // two column tiles per pass when the batch has 6 pairs per expert or more
-  // and 16 staged rows and the tables still leave room for two CTAs per SM;
-  // else one (fewer registers and no per-tile branch: Qwen-3-30B-A3B shape
-  // 32 tokens 84.7 -> 73.8 us, 64 tokens 92.9 -> 83.1, skewed 64 tokens 60.3
-  // -> 57.3; at 128 tokens two tiles are faster, 104.1 against 110.3)
-  const int64_t P = (int64_t)B * s->top_k;
-  if (P >= 6 * (int64_t)s->E &&
-      grp_layout(s->H, s->E, B * s->top_k, 2 * kGrpCols).total <= 110 * 1024)
-    return launch_grouped<kGrpUnroll, 2>(s, w, x, ids, B, h, err, st);
-  return launch_grouped<kGrpUnroll, 1>(s, w, x, ids, B, h, err, st);
+  // One column tile of 8 pairs per pass. Two tiles (16 staged rows, the codes
+  // decoded once for both) were faster only from about 96 tokens of the
+  // Qwen-3-30B-A3B shape while the kernel summed H in one chain; with the two
+  // halves of H summed apart, their registers spilled and the one-tile form
+  // with half-item shares is as fast or faster up to 128 tokens (96 tokens
+  // 87.5 us against 101.3 for the two-tile form).
+  return launch_grouped<kGrpUnroll>(s, w, x, ids, B, h, err, st);
 }
 
 }  // namespace wd

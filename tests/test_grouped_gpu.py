@@ -1,10 +1,11 @@
 """GPU parity of the expert-grouped moe_gate_up (moe_gate_up_grouped) against the oracle.
 
 The grouped kernel gives every (expert, 8 neurons) warp all the (token, slot)
-pairs routed to that expert as tensor-core MMA columns, 8 or 16 per pass. The
-cases below cover one and several column tiles, several passes over the
-weights (a hot expert), duplicate ids, invalid ids, the shapes of the target
-layers and the shapes the kernel refuses.
+pairs routed to that expert as tensor-core MMA columns, 8 per pass. The
+cases below cover one and several passes over the weights (a hot expert),
+whole items and half-items split over H, several items per CTA, duplicate
+ids, invalid ids, the shapes of the target layers and the shapes the kernel
+refuses.
 """
 import numpy as np
 import pytest
@@ -44,10 +45,12 @@ def tiny():
     return Layer(workload.SHAPES["tiny"])
 
 
-@pytest.mark.parametrize("B,routing", [(1, "uniform"), (8, "uniform"), (32, "uniform"), (64, "skewed")])
+@pytest.mark.parametrize("B,routing", [(1, "uniform"), (8, "uniform"), (32, "uniform"), (64, "skewed"),
+                                       (96, "uniform")])
 def test_grouped_q30_every_token(q30, B, routing):
     """Qwen-3-30B-A3B-shaped layer: every intermediate of every token. Skewed
-    routing at B=64 puts more than 16 pairs on the hot experts (several passes)."""
+    routing at B=64 puts more than 16 pairs on the hot experts (several passes);
+    96 tokens put 6 pairs on an expert on average."""
     x, ids, _ = workload.tokens(q30.shape, B, routing=routing, batch=B)
     h, err = _grouped(q30, x, ids)
     h_ref, _ = _h_ref(q30, x, ids)
@@ -57,7 +60,7 @@ def test_grouped_q30_every_token(q30, B, routing):
 
 def test_grouped_hot_expert_with_duplicates_several_passes(tiny):
     """Every slot of 40 tokens on expert 3 (duplicate ids in each token): 80 pairs
-    on one expert, 5 passes of 16 columns over its rows; the other experts idle."""
+    on one expert, 10 passes of 8 columns over its rows; the other experts idle."""
     B = 40
     x, _, _ = workload.tokens(tiny.shape, B, batch=21)
     ids = np.full((B, 2), 3, dtype=np.int32)
@@ -65,6 +68,19 @@ def test_grouped_hot_expert_with_duplicates_several_passes(tiny):
     h_ref, _ = _h_ref(tiny, x, ids)
     assert err == 0
     assert np.array_equal(h[:, 0], h[:, 1])  # a duplicate slot is the same pair twice
+    _check_h(h, h_ref)
+
+
+def test_grouped_several_items_per_cta(tiny):
+    """1600 tokens of the tiny layer: 3200 pairs in 8-column passes make about
+    800 work items, more than the persistent grid's CTAs, so CTAs run several
+    whole items one after the other (rows of 256: one 8-block group, no
+    half-items). Every intermediate against the oracle."""
+    B = 1600
+    x, ids, _ = workload.tokens(tiny.shape, B, batch=23)
+    h, err = _grouped(tiny, x, ids)
+    h_ref, _ = _h_ref(tiny, x, ids)
+    assert err == 0
     _check_h(h, h_ref)
 
 
@@ -81,13 +97,16 @@ def test_grouped_invalid_ids(tiny):
     _check_h(h, h_ref)
 
 
-def test_grouped_result_of_a_token_does_not_depend_on_the_batch(q30):
-    """Each (token, slot) column is an independent MMA column: a token's
-    intermediate is bit-identical whether it runs alone or in a batch of 32."""
-    B = 32
-    x, ids, _ = workload.tokens(q30.shape, B, batch=532)
+@pytest.mark.parametrize("B", [32, 29, 96, 128])
+def test_grouped_result_of_a_token_does_not_depend_on_the_batch(q30, B):
+    """Each (token, slot) column is an independent MMA column and every item
+    sums the lower and the upper half of H separately, whether it runs whole,
+    as a half-item split over two warps, so a token's intermediate is
+    bit-identical alone (every half-item split) and in a batch (29 and 32
+    tokens run half-item shares, 96 and 128 whole items)."""
+    x, ids, _ = workload.tokens(q30.shape, B, batch=500 + B)
     h, _ = _grouped(q30, x, ids)
-    for t in (0, 13, 31):
+    for t in (0, 13, B // 2, B - 1):
         h1, _ = _grouped(q30, x[t:t + 1], ids[t:t + 1])
         assert np.array_equal(h1[0], h[t]), t
 
