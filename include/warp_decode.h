@@ -26,14 +26,17 @@
  * LAYER KERNEL CHOICE (moe_layer, moe_layer_noalloc, moe_layer_routed with
  * ids_out), with P = B * top_k routed pairs, measured on GB300 under uniform
  * routing:
- *   gate/up grouped when P >= 2E (H < 4096), 8P >= 13E (H >= 4096);
- *   down grouped when    2P >= 5E (H < 6144), P >= 2E (H >= 6144);
+ *   gate/up grouped when 8P >= 13E (H < 4096), 2P >= 3E (H >= 4096);
+ *   down grouped when    4P >= 5E (I >= 3H), else 2P >= 5E (H < 6144),
+ *                        P >= 2E (H >= 6144);
  * each only where the grouped kernel takes the shape and batch. The choice
  * is reported by moe_layer_gate_up_kernel and moe_layer_down_kernel.
  * moe_layer_host has the ids on the host and counts the batch's distinct
  * valid experts U instead (E <= 256):
- *   gate/up grouped when P >= 2.15 U (H < 4096), P >= 1.95 U (H >= 4096);
- *   down grouped when    P >= 2.6 U (H < 6144), P >= 2.2 U (H >= 6144);
+ *   gate/up grouped when P >= 2 U (H < 4096), P >= 1.95 U (H >= 4096);
+ *   down grouped when    P >= 1.5 U (I >= 3H), else P >= 2.6 U (H < 6144),
+ *                        P >= 2.2 U (H >= 6144);
+ * both only when 4P >= 3E or P >= 4U (below 3E/4 pairs, heavy sharing only);
  * the same break-even points under uniform routing, and earlier where the
  * pairs crowd onto few experts (skewed routing); moe_layer_host_kernels
  * reports that choice.
@@ -148,8 +151,9 @@ moe_status moe_gate_up(const moe_shape* shape, const moe_weights* w, const uint1
  * ("Better MoE model inference with warp decode", [§How the two kernels
  * work]; the routed experts of [§Reorganized parallelism]). Arguments and
  * result as for moe_gate_up; the sums differ from moe_gate_up's only in
- * FP32 rounding order; a pair's result does not depend on the other pairs
- * of the batch. Returns MOE_ERR_UNSUPPORTED, launching nothing, unless
+ * FP32 rounding order (within each 32-element block, and the lower and the
+ * upper half of H summed apart and then added); a pair's result does not
+ * depend on the other pairs of the batch. Returns MOE_ERR_UNSUPPORTED, launching nothing, unless
  * H % 256 == 0, I % 64 == 0, E <= 256, gu_scales is 8-byte aligned and the
  * batch's pair lists fit in one CTA's shared memory.
  * moe_layer and the other layer entry points use this kernel by themselves
@@ -192,7 +196,7 @@ moe_status moe_down(const moe_shape* shape, const moe_weights* w, const uint16_t
 
 /*
  * moe_down_grouped -- moe_down computed by its expert-grouped kernel: one CTA
- * per 16 output rows o0..o0+15 serves every token of the batch. Its 8 warps
+ * per 16 output rows o0..o0+15 serves every token of the batch. Its 12 warps
  * take the batch's routed experts in turn; for each, a warp streams rows
  * o0..o0+15 of that expert's down matrix once and multiplies them on the
  * tensor cores (mma.sync m16n8k16, f16 operands, FP32 accumulation; rows are

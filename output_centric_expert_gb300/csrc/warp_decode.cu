@@ -153,20 +153,20 @@ moe_status gate_up_impl(const moe_shape* s, const moe_weights* w, const uint16_t
 // The form of moe_gate_up a layer entry point uses: the expert-grouped kernel
 // once the batch has enough pairs per expert, if the shape allows it. The
 // switch points are measured on GB300 in the layer (CUDA graph, cold L2,
-// uniform routing), with the per-token kernel at its four-CTA launch where
-// that applies and the grouped one at one column tile: per-token vs grouped
-// gate/up break even at about 30 tokens for the Qwen-3-30B-A3B shape (1.9 E
-// pairs; H = 2048: layer at 28 tokens 104.5 us per-token vs 109.7 with the
-// grouped gate/up, at 32 tokens 117.9 vs 116.3, at 36 128.2 vs 121.2), 25 for the
-// Qwen-3-235B-A22B shape (1.6 E; H = 4096: 24 tokens 354.9 us per-token vs
-// 361.1 grouped, 28 tokens 410.5 vs 380.9) and 52 for the DeepSeek-V3 shape
-// (1.6 E; H = 7168: 48 tokens 1655 vs 1850, 56 tokens 2097 vs 1999). The
-// longer rows make each (token, expert) pair dearer for the per-token kernel.
+// uniform routing, the down step per-token): per-token vs grouped gate/up
+// break even at about 25 tokens for the Qwen-3-30B-A3B shape (1.56 E pairs;
+// H = 2048: 24 tokens 95.2 us per-token vs 97.1 with the grouped gate/up, 26
+// tokens 101.1 vs 100.7, 28 tokens 104.5 vs 101.7), 24 for the
+// Qwen-3-235B-A22B shape (1.5 E; H = 4096: 22 tokens 331.0 vs 337.7, 24
+// tokens 356.2 vs 357.1, 26 tokens 390.3 vs 357.2), 6 for the Mixtral shape
+// (1.5 E; 5 tokens 221.4 vs 230.7, 6 tokens 259.4 vs 255.4) and 48 for the
+// DeepSeek-V3 shape (1.5 E; H = 7168: 44 tokens 1536.6 vs 1584.6, 48 tokens
+// 1653.4 vs 1659.8, 52 tokens 1985.0 vs 1728.5).
 GateUpForm layer_form(const moe_shape* s, const moe_weights* w, int32_t B) {
   if (!s) return GateUpForm::kPerToken;
   const int64_t pairs = (int64_t)B * s->top_k, E = s->E;
-  const bool shared = s->H >= 4096 ? 8 * pairs >= 13 * E  // 1.625 E pairs
-                                   : pairs >= 2 * E;      // 2 E
+  const bool shared = s->H >= 4096 ? 2 * pairs >= 3 * E    // 1.5 E pairs
+                                   : 8 * pairs >= 13 * E;  // 1.625 E
   if (shared && gate_up_grouped_supported(s, w, B)) return GateUpForm::kGrouped;
   return GateUpForm::kPerToken;
 }
@@ -207,12 +207,18 @@ moe_status down_impl(const moe_shape* s, const moe_weights* w, const uint16_t* h
 // Measured on GB300 (each kernel alone, CUDA graph, cold L2, uniform
 // routing), per-token vs grouped down break even at about 37 tokens for the
 // Qwen-3-30B-A3B shape (43.8 vs 46.4 us at 32, 52.2 vs 50.7 at 40), 33 for
-// the Qwen-3-235B-A22B shape, 8 for the Mixtral shape (2 E pairs) and 55 for
-// the DeepSeek-V3 shape (1.7 E).
+// the Qwen-3-235B-A22B shape and 55 for the DeepSeek-V3 shape (1.7 E). Rows
+// of the intermediate much longer than the output (I >= 3H: the Mixtral
+// shape's 14336 against 4096) make each token's down rows long for the
+// per-token kernel: there the grouped down wins from 1.25 E pairs (layer with
+// the per-token gate/up: 4 tokens 170.7 us per-token down vs 172.3 grouped,
+// 5 tokens 221.4 vs 204.3).
 DownForm layer_down_form(const moe_shape* s, const moe_weights* w, int32_t B) {
   if (!s) return DownForm::kPerToken;
   const int64_t pairs = (int64_t)B * s->top_k, E = s->E;
-  const bool shared = s->H >= 6144 ? pairs >= 2 * E : 2 * pairs >= 5 * E;
+  const bool shared = s->I >= 3 * (int64_t)s->H ? 4 * pairs >= 5 * E
+                      : s->H >= 6144           ? pairs >= 2 * E
+                                               : 2 * pairs >= 5 * E;
   if (shared && down_grouped_supported(s, w, B)) return DownForm::kGrouped;
   return DownForm::kPerToken;
 }
@@ -222,15 +228,19 @@ DownForm layer_down_form(const moe_shape* s, const moe_weights* w, int32_t B) {
 // distinct experts of the batch, so that a batch whose pairs crowd onto few
 // experts (skewed routing) takes the grouped kernels where they win. With
 // uniform routing U = E (1 - (1 - k/E)^B) on average, and the thresholds
-// reproduce the rules on P and E at the measured shapes: gate/up tau = 2.15
-// (H < 4096; Qwen-3-30B-A3B: 2.00-2.13 pairs per used expert at 28 tokens,
-// 2.19-2.39 at 32) or 1.95 (H >= 4096; Qwen-3-235B-A22B 1.90
-// at 24 tokens and 2.0 at 26, DeepSeek-V3 shape 1.92 at 48 and 2.01 at 52,
-// Mixtral shape 1.82 at 6 and 2.02 at 7); down
-// tau = 2.6 (H < 6144) or 2.2 (H >= 6144; DeepSeek-V3 shape 2.1 at 55
-// tokens). Skewed Qwen-3-30B-A3B batch of 32 tokens (43 used experts, 6 pairs
-// each): gate/up 45.0 us grouped against 73.8 per-token, down 34.9 against
-// 38.4.
+// reproduce the rules on P and E at the measured shapes: gate/up tau = 2.0
+// (H < 4096; Qwen-3-30B-A3B: 1.98 pairs per used expert at 24 tokens, 2.05
+// at 26) or 1.95 (H >= 4096; Qwen-3-235B-A22B 1.94 at 23 tokens and 1.98 at
+// 24, DeepSeek-V3 shape 1.92 at 48); down tau = 2.6 (H < 6144), 2.2 (H >=
+// 6144; DeepSeek-V3 shape 2.1 at 55 tokens) or 1.5 (I >= 3H; Mixtral shape
+// 1.46 at 4 tokens, 1.64 at 5). Below 3E/4 pairs the grouped kernels' fixed
+// costs (every CTA lists the pairs, stages activations) need more sharing
+// than that: they are taken there only from 4 pairs per used expert
+// (Qwen-3-30B-A3B skewed batches: 8 tokens, 64 pairs, 2.4 per used expert,
+// layer 34.7 us per-token vs 36.5 with the grouped gate/up; 12 tokens, 96
+// pairs, 45.8 us both grouped vs 50.3). Skewed Qwen-3-30B-A3B batch of 32
+// tokens (43 used experts, 6 pairs each): gate/up 40.6 us grouped against
+// 73.8 per-token, down 34.9 against 38.4.
 struct LayerForms {
   GateUpForm gate_up;
   DownForm down;
@@ -253,8 +263,11 @@ LayerForms layer_forms_for_ids(const moe_shape* s, const moe_weights* w, const i
     }
   }
   if (U == 0) return f;
-  const bool gu_shared = s->H >= 4096 ? 20 * P >= 39 * U : 20 * P >= 43 * U;
-  const bool dn_shared = s->H >= 6144 ? 5 * P >= 11 * U : 5 * P >= 13 * U;
+  const bool enough = 4 * P >= 3 * (int64_t)s->E || P >= 4 * U;
+  const bool gu_shared = enough && (s->H >= 4096 ? 20 * P >= 39 * U : P >= 2 * U);
+  const bool dn_shared = enough && (s->I >= 3 * (int64_t)s->H ? 2 * P >= 3 * U
+                                    : s->H >= 6144           ? 5 * P >= 11 * U
+                                                             : 5 * P >= 13 * U);
   if (gu_shared && gate_up_grouped_supported(s, w, B)) f.gate_up = GateUpForm::kGrouped;
   if (dn_shared && down_grouped_supported(s, w, B)) f.down = DownForm::kGrouped;
   return f;

@@ -190,23 +190,26 @@ def test_header_is_plain_c_and_links(tmp_path):
 
 def test_layer_gate_up_kernel_rule():
     """The library's statement of the layer's gate/up kernel (a host-only call):
-    the grouped kernel from B*top_k >= 2E (H < 4096) or 8*B*top_k >= 13E
+    the grouped kernel from 8*B*top_k >= 13E (H < 4096) or 2*B*top_k >= 3E
     (H >= 4096) when it takes the shape (H % 256, I % 64), the per-token kernel
-    otherwise. The GPU test test_layer_uses_the_grouped_kernel_from_2e_pairs
+    otherwise. The GPU test test_layer_uses_the_grouped_kernel_from_its_switch
     checks that the layer really runs the kernel reported here."""
     q30 = ops.make_shape(2048, 768, 128, 8)
-    assert ops.layer_gate_up_kernel(q30, 31) == "per_token"
-    assert ops.layer_gate_up_kernel(q30, 32) == "grouped"
+    assert ops.layer_gate_up_kernel(q30, 25) == "per_token"
+    assert ops.layer_gate_up_kernel(q30, 26) == "grouped"
+    q235 = ops.make_shape(4096, 1536, 128, 8)
+    assert ops.layer_gate_up_kernel(q235, 23) == "per_token"
+    assert ops.layer_gate_up_kernel(q235, 24) == "grouped"
     assert ops.layer_gate_up_kernel(ops.make_shape(2080, 768, 128, 8), 64) == "per_token"
     assert ops.layer_gate_up_kernel(ops.make_shape(2048, 96, 128, 8), 64) == "per_token"
-    assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 7) == "per_token"
-    assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 8) == "grouped"
+    assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 6) == "per_token"
+    assert ops.layer_gate_up_kernel(ops.make_shape(256, 128, 8, 2), 7) == "grouped"
     for (H, I, E, k) in [(2048, 768, 128, 8), (4096, 1536, 128, 8), (7168, 2048, 256, 8),
                          (4096, 14336, 8, 2), (256, 128, 8, 2), (768, 192, 5, 3)]:
         sh = ops.make_shape(H, I, E, k)
-        for B in (1, 2, 5, 7, 8, 16, 17, 31, 32, 39, 40, 64, 65, 256):
+        for B in (1, 2, 5, 6, 7, 8, 16, 17, 23, 24, 25, 26, 39, 40, 64, 65, 256):
             P = B * k
-            shared = (8 * P >= 13 * E) if H >= 4096 else (P >= 2 * E)
+            shared = (2 * P >= 3 * E) if H >= 4096 else (8 * P >= 13 * E)
             want = "grouped" if (shared and H % 256 == 0 and I % 64 == 0 and E <= 256) else "per_token"
             assert ops.layer_gate_up_kernel(sh, B) == want, (H, I, E, k, B)
     # misaligned scales keep the per-token kernel; a bad shape is an error
@@ -221,18 +224,19 @@ def test_layer_gate_up_kernel_rule():
 def test_layer_host_kernel_choice():
     """moe_layer_host picks its kernels from the batch's own ids: pairs per used
     expert against the measured break-even points. Uniform routing gives the
-    same choice as the rules on B (Qwen-3-30B-A3B shape: per-token at 16 tokens,
-    grouped gate/up from 32, both grouped from 40); a skewed batch of 32 tokens,
-    its pairs on a few dozen
-    experts, takes the grouped kernels; all on one expert likewise; no valid id
-    keeps the per-token kernels. Host-only."""
+    same choice as the rules on B (Qwen-3-30B-A3B shape: per-token up to 24
+    tokens, grouped gate/up from 28, both grouped from 40); a skewed batch of 32
+    tokens, its pairs on a few dozen experts, takes the grouped kernels; a skewed
+    batch of 8 tokens (64 pairs, under 3E/4, and fewer than 4 per used expert)
+    keeps the per-token ones; all on one expert takes the grouped ones; no
+    valid id keeps the per-token kernels. Host-only."""
     from output_centric_expert_gb300 import workload
     q30 = workload.SHAPES["q30"]
     sh = ops.make_shape(q30.H, q30.I, q30.E, q30.top_k)
-    for B in (8, 16, 28):  # 28 tokens: 2.13 pairs per used expert
+    for B in (8, 16, 24):  # 24 tokens: 1.98 pairs per used expert
         ids = workload.tokens(q30, B, seed=0, batch=0, routing="uniform")[1]
         assert ops.layer_host_kernels(sh, ids) == ("per_token", "per_token"), B
-    for B in (32, 36):  # 2.29 and 2.46 pairs per used expert
+    for B in (28, 32, 36):  # 2.13, 2.29 and 2.46 pairs per used expert
         ids = workload.tokens(q30, B, seed=0, batch=0, routing="uniform")[1]
         assert ops.layer_host_kernels(sh, ids) == ("grouped", "per_token"), B
         assert ops.layer_gate_up_kernel(sh, B) == "grouped" and ops.layer_down_kernel(sh, B) == "per_token"
@@ -245,31 +249,44 @@ def test_layer_host_kernel_choice():
         U = len(np.unique(ids))
         assert 256 >= 2.6 * U, U  # the skewed batches crowd onto few experts
         assert ops.layer_host_kernels(sh, ids) == ("grouped", "grouped")
+        ids = workload.tokens(q30, 8, seed=0, batch=b, routing="skewed")[1]
+        assert 2.0 * len(np.unique(ids)) <= 64 < 4 * len(np.unique(ids))  # 2.0-2.4 per used expert
+        assert ops.layer_host_kernels(sh, ids) == ("per_token", "per_token")
     one = np.full((8, 8), 5, dtype=np.int32)  # 64 pairs on expert 5 (duplicates within tokens)
     assert ops.layer_host_kernels(sh, one) == ("grouped", "grouped")
     none = np.full((8, 8), -1, dtype=np.int32)
     assert ops.layer_host_kernels(sh, none) == ("per_token", "per_token")
-    # the thresholds in pairs per used expert, at a boundary (top_k = 1): down
-    # grouped from 2.6 per expert (13 pairs on 5 experts; 12 on 5 is 2.4), gate/up
-    # from 2.15 (43 pairs on 20 experts; 42 on 20 is 2.1)
-    sh1 = ops.make_shape(2048, 768, 128, 1)
+    # the thresholds in pairs per used expert, at a boundary (top_k = 1, 8 experts,
+    # so that 3E/4 = 6 pairs): down grouped from 2.6 per expert (13 pairs on 5
+    # experts; 12 on 5 is 2.4), gate/up from 2.0 (10 on 5; 9 on 5 is 1.8)
+    sh1 = ops.make_shape(2048, 768, 8, 1)
     ids13 = np.array([[e] for e in [0, 1, 2, 3, 4] * 2 + [0, 1, 2]], dtype=np.int32)
-    ids12 = ids13[:12]
     assert ops.layer_host_kernels(sh1, ids13) == ("grouped", "grouped")
-    assert ops.layer_host_kernels(sh1, ids12) == ("grouped", "per_token")
-    ids43 = np.array([[e] for e in list(range(20)) * 2 + [0, 1, 2]], dtype=np.int32)
-    assert ops.layer_host_kernels(sh1, ids43) == ("grouped", "per_token")
-    assert ops.layer_host_kernels(sh1, ids43[:42]) == ("per_token", "per_token")
+    assert ops.layer_host_kernels(sh1, ids13[:12]) == ("grouped", "per_token")
+    assert ops.layer_host_kernels(sh1, ids13[:10]) == ("grouped", "per_token")
+    assert ops.layer_host_kernels(sh1, ids13[:9]) == ("per_token", "per_token")
+    # below 3E/4 pairs only 4 pairs per used expert or more count: 13 pairs on 5
+    # of 128 experts keep the per-token kernels, 20 on 5 take the grouped ones
+    sh1b = ops.make_shape(2048, 768, 128, 1)
+    assert ops.layer_host_kernels(sh1b, ids13) == ("per_token", "per_token")
+    ids20 = np.array([[e] for e in [0, 1, 2, 3, 4] * 4], dtype=np.int32)
+    assert ops.layer_host_kernels(sh1b, ids20) == ("grouped", "grouped")
     # longer rows: gate/up from 1.95 pairs per expert (H >= 4096), down from 2.2 (H >= 6144)
-    sh4 = ops.make_shape(4096, 1536, 128, 1)
+    sh4 = ops.make_shape(4096, 1536, 8, 1)
     ids9 = np.array([[e] for e in [0, 1, 2, 3] * 2 + [0]], dtype=np.int32)  # 9 on 4: 2.25
     assert ops.layer_host_kernels(sh4, ids9) == ("grouped", "per_token")
+    sh4b = ops.make_shape(4096, 1536, 32, 1)
     ids39 = np.array([[e] for e in list(range(20)) + list(range(19))], dtype=np.int32)  # 39 on 20
-    assert ops.layer_host_kernels(sh4, ids39)[0] == "grouped"  # 1.95 pairs per used expert
-    assert ops.layer_host_kernels(sh4, ids39[:38])[0] == "per_token"  # 1.9
-    sh7 = ops.make_shape(7168, 2048, 256, 1)
+    assert ops.layer_host_kernels(sh4b, ids39)[0] == "grouped"  # 1.95 pairs per used expert
+    assert ops.layer_host_kernels(sh4b, ids39[:38])[0] == "per_token"  # 1.9
+    sh7 = ops.make_shape(7168, 2048, 8, 1)
     assert ops.layer_host_kernels(sh7, ids9) == ("grouped", "grouped")
     assert ops.layer_host_kernels(sh7, ids9[:8]) == ("grouped", "per_token")  # 2.0 per expert
+    # intermediate rows of 3H and more: down from 1.5 pairs per expert
+    shm = ops.make_shape(4096, 14336, 8, 1)
+    ids6 = np.array([[e] for e in [0, 1, 2, 3, 0, 1]], dtype=np.int32)  # 6 on 4
+    assert ops.layer_host_kernels(shm, ids6) == ("per_token", "grouped")
+    assert ops.layer_host_kernels(shm, ids6[:5]) == ("per_token", "per_token")  # 5 < 3E/4
     # E > 256: beyond the grouped kernels
     big = ops.make_shape(2048, 768, 257, 8)
     assert ops.layer_host_kernels(big, one) == ("per_token", "per_token")
@@ -279,17 +296,18 @@ def test_layer_host_kernel_choice():
 
 def test_layer_down_kernel_choice():
     """The layer's down kernel: the expert-grouped one from 2.5E pairs (2E for
-    rows of 6144 and more) when
-    it takes the shape (I % 256 == 0, E <= 256) and batch (up to 64 tokens for
+    rows of 6144 and more; 1.25E where the intermediate rows are 3H or longer)
+    when it takes the shape (I % 256 == 0, E <= 256) and batch (up to 64 tokens for
     these shapes; never beyond 128), the per-token one otherwise; the library
     answers on the host, without a GPU."""
     for (H, I, E, k) in [(2048, 768, 128, 8), (4096, 1536, 128, 8), (7168, 2048, 256, 8),
                          (4096, 14336, 8, 2), (256, 128, 8, 2), (64, 256, 6, 3),
                          (2048, 768, 257, 8)]:
         sh = ops.make_shape(H, I, E, k)
-        for B in (1, 2, 3, 9, 10, 15, 16, 17, 32, 39, 40, 63, 64, 129, 256):
+        for B in (1, 2, 3, 4, 5, 9, 10, 15, 16, 17, 32, 39, 40, 63, 64, 129, 256):
             P = B * k
-            shared = (P >= 2 * E) if H >= 6144 else (2 * P >= 5 * E)
+            shared = (4 * P >= 5 * E) if I >= 3 * H else \
+                (P >= 2 * E) if H >= 6144 else (2 * P >= 5 * E)
             want = "grouped" if (shared and I % 256 == 0 and E <= 256 and B <= 64) \
                 else "per_token"
             assert ops.layer_down_kernel(sh, B) == want, (H, I, E, k, B)

@@ -114,6 +114,26 @@ def test_layer_switches_down_kernel_at_2_5e_pairs(q30):
         assert np.array_equal(y.cpu().numpy(), want), B
 
 
+def test_layer_switches_down_kernel_for_long_intermediate_rows():
+    """Mixtral-shaped layer (I = 14336, three and a half times H): moe_layer's y
+    equals moe_down's at 4 tokens (8 pairs on 8 experts) and moe_down_grouped's
+    from 4 * B * top_k >= 5E (5 tokens), bit for bit, on the intermediate the
+    layer itself produced; the gate/up step stays per-token below 2 * B * top_k
+    = 3E (6 tokens)."""
+    s = workload.SHAPES["mixtral"]
+    layer = Layer(s, oracle_experts=[])
+    for B, want in ((4, ("per_token", "per_token")), (5, ("per_token", "grouped")),
+                    (6, ("grouped", "grouped"))):
+        assert (ops.layer_gate_up_kernel(layer.sh, B), ops.layer_down_kernel(layer.sh, B)) == want
+        x, ids, w = workload.tokens(s, B, batch=650 + B)
+        h = torch.empty((B, s.top_k, s.I), dtype=torch.int16, device="cuda")
+        y = torch.empty((B, s.H), dtype=torch.float32, device="cuda")
+        ops.moe_layer(layer.dev, _dev(x.view(np.int16)), _dev(ids), _dev(w), h, y)
+        torch.cuda.synchronize()
+        yd = _down(layer, h.cpu().numpy().view(np.uint16), ids, w, grouped=(want[1] == "grouped"))
+        assert np.array_equal(y.cpu().numpy(), yd), B
+
+
 @pytest.mark.parametrize("B,routing,batch", [(32, "skewed", 0), (32, "skewed", 3), (16, "skewed", 1),
                                              (32, "uniform", 0), (40, "uniform", 2)])
 def test_host_entry_point_chooses_from_its_ids(q30, B, routing, batch):

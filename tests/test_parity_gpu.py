@@ -170,8 +170,8 @@ def test_q235_sampled_tokens(q235, B):
     assert np.all(np.isfinite(y))
 
 
-@pytest.mark.parametrize("name,E,B", [("dsv3", 16, 12), ("mixtral", 8, 6), ("dsv3", 16, 1),
-                                      ("mixtral", 8, 1), ("q235", 8, 1)])
+@pytest.mark.parametrize("name,E,B", [("dsv3", 16, 12), ("mixtral", 8, 6), ("mixtral", 8, 4),
+                                      ("dsv3", 16, 1), ("mixtral", 8, 1), ("q235", 8, 1)])
 def test_shape_variants(name, E, B):
     """DeepSeek-V3-shaped (H=7168: partial row segments) and Mixtral-shaped
     (I=14336: a 57 KB intermediate per token) layers, with fewer experts than the
@@ -293,10 +293,10 @@ def test_batch_equals_tokens_one_at_a_time(request, form, which, B, routing):
         assert np.array_equal(y1[0], y[t]), t
 
 
-def test_layer_uses_the_grouped_kernel_from_2e_pairs(q30):
-    """moe_layer's intermediate equals moe_gate_up's below B*top_k = 2E and
-    moe_gate_up_grouped's from there on (Qwen-3-30B-A3B shape: 32 tokens)."""
-    for B in (31, 32):
+def test_layer_uses_the_grouped_kernel_from_its_switch(q30):
+    """moe_layer's intermediate equals moe_gate_up's below 8*B*top_k = 13E and
+    moe_gate_up_grouped's from there on (Qwen-3-30B-A3B shape: 26 tokens)."""
+    for B in (25, 26):
         x, ids, w = workload.tokens(q30.shape, B, batch=700 + B)
         _, h = _run_layer(q30, x, ids, w)
         hp = torch.empty((B, 8, q30.shape.I), dtype=torch.int16, device="cuda")
@@ -304,8 +304,9 @@ def test_layer_uses_the_grouped_kernel_from_2e_pairs(q30):
         ops.moe_gate_up(q30.dev, _dev(x.view(np.int16)), _dev(ids), hp)
         ops.moe_gate_up_grouped(q30.dev, _dev(x.view(np.int16)), _dev(ids), hg)
         torch.cuda.synchronize()
-        assert ops.layer_gate_up_kernel(q30.sh, B) == ("grouped" if B * 8 >= 2 * 128 else "per_token")
-        want = (hg if B * 8 >= 2 * 128 else hp).cpu().numpy().view(np.uint16)
+        grouped = 8 * B * 8 >= 13 * 128
+        assert ops.layer_gate_up_kernel(q30.sh, B) == ("grouped" if grouped else "per_token")
+        want = (hg if grouped else hp).cpu().numpy().view(np.uint16)
         assert np.array_equal(h, want), B
 
 
