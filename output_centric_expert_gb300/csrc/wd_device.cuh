@@ -157,10 +157,15 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
         "f"(c[2]), "f"(c[3]));
 }
 
-// 16 codes (half of one of two adjacent 32-element blocks), not allocated in L1.
+// 16 codes (half of one of two adjacent 32-element blocks), not allocated in
+// L1. A warp's load covers 64 bytes of each of 8 rows and its next three loads
+// the rest of the same 256 bytes, so the L2 fetches 256-byte segments
+// (grouped gate/up alone: Qwen-3-30B-A3B 32 tokens 68.7 -> 68.4 us,
+// Qwen-3-235B-A22B 32 tokens 237.3 -> 235.4, Mixtral-shaped 16 tokens 159.5 ->
+// 158.4; 128-byte segments: no change).
 __device__ __forceinline__ uint4 ld_codes16(const uint8_t* p) {
   uint4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
       : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
       : "l"(p));
   return r;
