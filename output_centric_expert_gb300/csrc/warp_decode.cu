@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     moe_route_kernel(const float* __restrict__ logits, int32_t* __restrict__ ids,
                      float* __restrict__ wts, int B, int E, int top_k) {
+  launch_dependents();  // moe_layer_routed's gate/up kernel waits for the ids itself
   const int t = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   if (t >= B) return;
   const int lane = threadIdx.x & 31;
@@ -143,7 +144,7 @@ moe_status gate_up_impl(const moe_shape* s, const moe_weights* w, const uint16_t
     return MOE_ERR_ALIGN;
   }
   if (form == GateUpForm::kGrouped)
-    rc = launch_gate_up_grouped(s, w, x, ids, B, h, err, st);
+    rc = launch_gate_up_grouped(s, w, x, ids, B, h, err, st, route.dependent);
   else
     rc = launch_gate_up_kernels(s, w, x, ids, B, h, err, st, route);
   if (rc != MOE_OK) return rc;
@@ -406,19 +407,24 @@ extern "C" moe_status moe_layer_routed(const moe_shape* shape, const moe_weights
   cudaStream_t st = (cudaStream_t)stream;
   if (ids_out) {
     // The routing has a home: route every token once into it, then run the
-    // layer on it (Q30 B=32: 127 us, against 157 us when every CTA of both
-    // kernels routes its token itself before it can request any weights).
+    // layer on it (Q30 B=32: 112.1 us, moe_layer on the same ids 108.6, against
+    // 161.2 us when every CTA of both kernels routes its token itself before it
+    // can request any weights).
     const unsigned grid = (unsigned)((B + kWarpsPerCta - 1) / kWarpsPerCta);
     moe_route_kernel<<<grid, kThreads, 0, st>>>(logits, ids_out, wts_out, B, shape->E,
                                                  shape->top_k);
     if ((rc = launch_status("moe_route launch")) != MOE_OK) return rc;
-    rc = gate_up_impl(shape, w, x, ids_out, B, h_scratch, err_flag, st, kNoRoute,
+    // the gate/up kernel is a programmatic dependent of the router: its CTAs
+    // are resident when the ids are written (B=1 16.1 -> 14.9 us, B=32 113.6 ->
+    // 112.1)
+    const RouteArgs after_router = {nullptr, true};
+    rc = gate_up_impl(shape, w, x, ids_out, B, h_scratch, err_flag, st, after_router,
                       layer_form(shape, w, B));
     if (rc != MOE_OK) return rc;
     return down_impl(shape, w, h_scratch, ids_out, wts_out, B, y, err_flag, st, true, nullptr,
                      layer_down_form(shape, w, B));
   }
-  const RouteArgs route = {logits};
+  const RouteArgs route = {logits, false};
   rc = gate_up_impl(shape, w, x, nullptr, B, h_scratch, err_flag, st, route);
   if (rc != MOE_OK) return rc;
   return down_impl(shape, w, h_scratch, nullptr, nullptr, B, y, err_flag, st, true, logits);

@@ -65,9 +65,11 @@ constexpr int kRouteMaxE = 256;
 
 struct RouteArgs {
   const float* logits;  // [B][E], or nullptr: the ids/wts arrays are the routing
+  bool dependent;       // launched as a programmatic dependent of the router kernel
+                        // that writes the ids (the kernel waits before reading them)
 };
 
-constexpr RouteArgs kNoRoute = {nullptr};
+constexpr RouteArgs kNoRoute = {nullptr, false};
 
 // ------------------------------------------------------ host helpers (shared) --
 // Defined with the C-ABI entry points; one error message per calling thread.

@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     e_lane = __shfl_sync(0xFFFFFFFFu, rid, lane < nslots ? j0 + lane : 0);
     if (lane >= nslots) e_lane = -1;
   } else {
+    wait_prerequisite();  // the ids are complete from here on (a router may write them)
     e_lane = (lane < nslots) ? __ldg(ids + (size_t)t * top_k + j0 + lane) : -1;
   }
 
@@ -146,8 +147,23 @@ moe_status launch_gate_up(const moe_shape* s, const moe_weights* w, const uint16
   if (rc != MOE_OK) return rc;
   const int groups = (s->top_k + SPW - 1) / SPW;
   const dim3 grid((unsigned)(B * groups), (unsigned)(s->I / kWarpsPerCta));
-  moe_gate_up_kernel<SPW, NSEG, FULL, KH, MINB><<<grid, kThreads, smem, st>>>(
-      w->gu_codes, w->gu_scales, x, ids, h, err, s->H, s->I, s->E, s->top_k, route);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = route.dependent ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_gate_up_kernel<SPW, NSEG, FULL, KH, MINB>,
+                                           w->gu_codes, w->gu_scales, x, ids, h, err, s->H,
+                                           s->I, s->E, s->top_k, route);
+  if (e != cudaSuccess) {
+    set_error("moe_gate_up launch", e);
+    return MOE_ERR_CUDA;
+  }
   return MOE_OK;
 }
 

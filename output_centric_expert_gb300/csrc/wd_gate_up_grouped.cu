@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     s_run[i] = 0;
   }
   for (int i = tid; i < kWarpsPerCta * E; i += kThreads) s_wc[i] = 0;
+  wait_prerequisite();  // the ids are complete from here on (a router may write them)
   __syncthreads();
   for (int p = tid; p < P; p += kThreads) {
     const int id = __ldg(ids + p);
@@ -481,13 +482,28 @@ __global__ void __launch_bounds__(kThreads, 2)
 template <int UNR>
 moe_status launch_grouped(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                           const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool dependent) {
   const size_t smem = grp_layout(s->H, s->E, B * s->top_k).total;
   moe_status rc = allow_smem(moe_gate_up_grouped_kernel<UNR>, smem);
   if (rc != MOE_OK) return rc;
   const unsigned grid = (unsigned)(2 * sm_count());
-  moe_gate_up_grouped_kernel<UNR><<<grid, kThreads, smem, st>>>(
-      w->gu_codes, w->gu_scales, x, ids, h, err, s->H, s->I, s->E, s->top_k, B);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, moe_gate_up_grouped_kernel<UNR>, w->gu_codes,
+                                           w->gu_scales, x, ids, h, err, s->H, s->I, s->E,
+                                           s->top_k, B);
+  if (e != cudaSuccess) {
+    set_error("moe_gate_up_grouped launch", e);
+    return MOE_ERR_CUDA;
+  }
   return MOE_OK;
 }
 
@@ -503,14 +519,14 @@ bool gate_up_grouped_supported(const moe_shape* s, const moe_weights* w, int32_t
 
 moe_status launch_gate_up_grouped(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                                   const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, bool dependent) {
   // One column tile of 8 pairs per pass. Two tiles (16 staged rows, the codes
   // decoded once for both) were faster only from about 96 tokens of the
   // Qwen-3-30B-A3B shape while the kernel summed H in one chain; with the two
   // halves of H summed apart, their registers spilled and the one-tile form
   // with half-item shares is as fast or faster up to 128 tokens (96 tokens
   // 87.5 us against 101.3 for the two-tile form).
-  return launch_grouped<kGrpUnroll>(s, w, x, ids, B, h, err, st);
+  return launch_grouped<kGrpUnroll>(s, w, x, ids, B, h, err, st, dependent);
 }
 
 }  // namespace wd

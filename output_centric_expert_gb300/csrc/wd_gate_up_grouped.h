@@ -14,9 +14,11 @@ namespace wd {
 bool gate_up_grouped_supported(const moe_shape* s, const moe_weights* w, int32_t B);
 
 // Launch it on `st` (expert ids only, no routing from logits); the arguments
-// have been validated by the entry point. Returns MOE_OK or an error status.
+// have been validated by the entry point. dependent: launch as a programmatic
+// dependent of the preceding kernel (the router that writes the ids; the
+// kernel waits for it before reading them). Returns MOE_OK or an error status.
 moe_status launch_gate_up_grouped(const moe_shape* s, const moe_weights* w, const uint16_t* x,
                                   const int32_t* ids, int32_t B, uint16_t* h, int32_t* err,
-                                  cudaStream_t st);
+                                  cudaStream_t st, bool dependent = false);
 
 }  // namespace wd
