@@ -60,9 +60,10 @@ def q30():
 
 
 # B=1, 2, 4 and 32 run moe_down with 1 x 8, 2 x 4, 4 x 2 and 8 x 1 outputs x units per lane;
-# with ids_out/wts_out given the routing is computed once into them, without them every
-# CTA of both kernels routes its token itself
-@pytest.mark.parametrize("B", [1, 2, 4, 32])
+# with ids_out/wts_out given the routing is computed once into them (the gate/up kernel then
+# runs as a programmatic dependent of the router; from 26 tokens the grouped one, from 40 the
+# grouped down too), without them every CTA of both kernels routes its token itself
+@pytest.mark.parametrize("B", [1, 2, 4, 26, 32, 64])
 @pytest.mark.parametrize("keep_routing", [True, False])
 def test_layer_from_logits(q30, B, keep_routing):
     """moe_layer_routed == moe_layer fed moe_route's routing (bit for bit) when
