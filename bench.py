@@ -124,6 +124,17 @@ def kernel_source_sha(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
+def ncu_traffic_stale(kernel: str, workload: str) -> bool:
+    """Whether the committed ncu summary for the kernel and workload was taken
+    on an earlier source of the kernel (so its bytes are not reported)."""
+    p = os.path.join(REPO, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return False
+    with open(p) as f:
+        ent = json.load(f).get(kernel, {}).get(workload)
+    return bool(ent) and ent.get("kernel_sha") != kernel_source_sha(kernel)
+
+
 def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel source; else None."""
@@ -618,9 +629,13 @@ def run_ours(args, wl, rank, world, local_rank):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": gu_gbs / peak,
                      "algorithmic_bytes_per_launch": gu_launch_bytes,
                      "traffic": traffic,
-                     "traffic_note": None if traffic is None else
-                     f"mean of the ncu-captured launches, whose own algorithmic bytes average "
-                     f"{traffic_alg} (ratio {traffic / traffic_alg:.4f}); profiles/traffic.json"},
+                     "traffic_note": (
+                         f"mean of the ncu-captured launches, whose own algorithmic bytes average "
+                         f"{traffic_alg} (ratio {traffic / traffic_alg:.4f}); profiles/traffic.json"
+                         if traffic is not None else
+                         "the capture in profiles/traffic.json was taken on an earlier source of "
+                         "this kernel, so it is not reported"
+                         if ncu_traffic_stale(gu_kernel, wl.name) else None)},
         "cpu_baseline": cpu,
         "cpu_baseline_all_cores": cpu_all,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,

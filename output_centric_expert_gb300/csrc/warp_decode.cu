@@ -415,8 +415,9 @@ extern "C" moe_status moe_layer_routed(const moe_shape* shape, const moe_weights
                                                  shape->top_k);
     if ((rc = launch_status("moe_route launch")) != MOE_OK) return rc;
     // the gate/up kernel is a programmatic dependent of the router: its CTAs
-    // are resident when the ids are written (B=1 16.1 -> 14.9 us, B=32 113.6 ->
-    // 112.1)
+    // are resident when the ids are written (B=1 16.1 -> 15.8 us, B=32 113.6 ->
+    // 112.1). It releases moe_down, which reads the ids before its own wait,
+    // only after its wait for the router.
     const RouteArgs after_router = {nullptr, true};
     rc = gate_up_impl(shape, w, x, ids_out, B, h_scratch, err_flag, st, after_router,
                       layer_form(shape, w, B));

@@ -49,13 +49,16 @@ __global__ void __launch_bounds__(kThreads, MINB)
   const int nblk = H >> 5;
   const int nslots = min(SPW, top_k - j0);
 
-  launch_dependents();
-
-  // lane s < nslots holds the expert id of slot s; -1 marks "no slot"
+  // lane s < nslots holds the expert id of slot s; -1 marks "no slot".
+  // moe_down is launched as a dependent of this kernel and reads the ids
+  // before its own wait, so the dependents are released only once the ids
+  // are complete (after the wait for a router that writes them; at once
+  // otherwise).
   int e_lane;
   if (route.logits) {  // route the token here, from its logits (every warp routes: a
                        // barrier here, to route once per CTA, slowed the kernel for
                        // the 235B-shaped layer even when no logits are given)
+    launch_dependents();
     int rid;
     float rw;
     warp_route(route.logits + (size_t)t * E, E, top_k, rid, rw);
@@ -63,6 +66,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     if (lane >= nslots) e_lane = -1;
   } else {
     wait_prerequisite();  // the ids are complete from here on (a router may write them)
+    launch_dependents();
     e_lane = (lane < nslots) ? __ldg(ids + (size_t)t * top_k + j0 + lane) : -1;
   }
 

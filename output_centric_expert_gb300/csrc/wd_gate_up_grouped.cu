@@ -152,8 +152,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int nblk = H >> 5;
   const int RS = grp_row_bytes(H);
 
-  launch_dependents();
-
   // ---- pair lists by expert and the work items (the same in every CTA) ----
   for (int i = tid; i < E; i += kThreads) {
     s_cnt[i] = 0;
@@ -161,6 +159,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   for (int i = tid; i < kWarpsPerCta * E; i += kThreads) s_wc[i] = 0;
   wait_prerequisite();  // the ids are complete from here on (a router may write them)
+  // moe_down, a dependent of this kernel, reads the ids before its own wait:
+  // it is released only now
+  launch_dependents();
   __syncthreads();
   for (int p = tid; p < P; p += kThreads) {
     const int id = __ldg(ids + p);
