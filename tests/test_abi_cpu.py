@@ -294,6 +294,35 @@ def test_layer_host_kernel_choice():
         ops.layer_host_kernels(ops.make_shape(100, 768, 128, 8), one)
 
 
+def test_layer_host_kernel_rule_on_random_batches():
+    """moe_layer_host_kernels follows the rule the header states, on random
+    batches of up to 64 tokens whose ids crowd onto random subsets of the
+    experts (some slots invalid): with P = B*top_k pairs and U distinct valid
+    experts, either step is grouped only when 4P >= 3E or P >= 4U, gate/up
+    when P >= 2U (H < 4096) or 20P >= 39U (H >= 4096), down when 2P >= 3U
+    (I >= 3H), else 5P >= 13U (H < 6144) or 5P >= 11U (H >= 6144). The shapes
+    are ones both grouped kernels take at 64 tokens (checked). Host-only."""
+    rng = np.random.default_rng(7)
+    shapes = [(2048, 768, 128, 8), (4096, 1536, 128, 8), (7168, 2048, 256, 8),
+              (4096, 14336, 8, 2), (2048, 768, 16, 4), (7168, 2048, 64, 2)]
+    for (H, I, E, k) in shapes:
+        sh = ops.make_shape(H, I, E, k)
+        assert ops.layer_gate_up_kernel(sh, 64) == "grouped" and ops.layer_down_kernel(sh, 64) == "grouped"
+        for _ in range(60):
+            B = int(rng.integers(1, 65))
+            pool = rng.choice(E, size=int(rng.integers(1, E + 1)), replace=False)
+            ids = rng.choice(pool, size=(B, k)).astype(np.int32)
+            ids[rng.random((B, k)) < 0.05] = -1
+            P = B * k
+            U = len(np.unique(ids[ids >= 0]))
+            enough = U > 0 and (4 * P >= 3 * E or P >= 4 * U)
+            gu = enough and ((20 * P >= 39 * U) if H >= 4096 else (P >= 2 * U))
+            dn = enough and ((2 * P >= 3 * U) if I >= 3 * H else
+                             (5 * P >= 11 * U) if H >= 6144 else (5 * P >= 13 * U))
+            want = ("grouped" if gu else "per_token", "grouped" if dn else "per_token")
+            assert ops.layer_host_kernels(sh, ids) == want, (H, I, E, k, B, U)
+
+
 def test_layer_down_kernel_choice():
     """The layer's down kernel: the expert-grouped one from 2.5E pairs (2E for
     rows of 6144 and more; 1.25E where the intermediate rows are 3H or longer)
