@@ -67,8 +67,9 @@ moe_status launch_gate_up_kernels(const moe_shape* s, const moe_weights* w, cons
   int spw = small_batch_spw(B, s->top_k, s->I, nseg), ctas_per_sm = 3;
   if (spw == 0) {
     spw = pick_spw(B, s->top_k, s->I);
-    // Below the grouped switch (1.5 E pairs for H = 2048, where 8 slots at
-    // three CTAs win from 28 tokens; 1.625 E pairs from H = 4096), for the
+    // Up to 1.5 E pairs for H = 2048 (where 8 slots at three CTAs win from 28
+    // tokens) and below 1.625 E pairs from H = 4096 (the batches the layer runs
+    // this kernel on, and moe_gate_up's own calls a little beyond), for the
     // rows compiled with fixed length: four CTAs
     // per SM (64 registers) with 4 (slot, segment) units per warp (H = 2048;
     // H = 4096 up to E pairs or with top_k < 4) or 8 (H = 4096 beyond E

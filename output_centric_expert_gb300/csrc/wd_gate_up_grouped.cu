@@ -60,8 +60,8 @@
 // (about 60 % of peak against 47 % for DRAM, ncu, Qwen-3-30B-A3B shape at 32
 // tokens); 16 bytes per lane and the swap cut the kernel's time there from
 // 95.5 to 83.7 us with bit-identical results. Measured on GB300, in the
-// layer, it is faster than the per-token kernel from about 30 tokens
-// (Qwen-3-30B-A3B shape) or 25 tokens (Qwen-3-235B-A22B shape) under uniform
+// layer, it is faster than the per-token kernel from about 25 tokens
+// (Qwen-3-30B-A3B shape) or 24 tokens (Qwen-3-235B-A22B shape) under uniform
 // routing, and far ahead at 32 skewed tokens.
 #include "wd_device.cuh"
 #include "wd_gate_up_grouped.h"
